@@ -1,0 +1,17 @@
+"""fp64 CPU oracle for the attention hot path (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package; the library never does.
+"""
+
+from .attention import (  # noqa: F401
+    admissible_keys,
+    attention,
+    attention_head,
+    chunk_partials,
+    combine,
+    compositions,
+    decode,
+    online_attention_head,
+    online_merge_scores,
+)

@@ -1,0 +1,282 @@
+"""Plain fp64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code, header, table or helper with the CUDA library; it receives the exact
+bf16 input values (widened to fp64) and produces the values the GPU results are
+compared against.
+
+What it computes, and where the pages define it
+-----------------------------------------------
+* ``attention`` -- the plain definition S = scale * Q K^T, P = softmax(S),
+  O = P V, one explicit score row per query (xuesongtap.github.io
+  "flash-attention" page, §1 equation for S, P, O; triton-tutorial
+  "8. FlashAttention 实战", §8.1 ``naive_attention``).  The log-sum-exp saved
+  per row is m + log(l) in natural log of the *scaled* scores (xuesongtap §3,
+  "前向额外保存逐行的 log-sum-exp"; triton-tutorial §8.8.2).  Causal keeps key
+  j <= i (triton-tutorial §8.7.1, diagonal-block mask ``offs_m >= offs_n``),
+  masked scores are -inf (xuesongtap §2.2, last paragraph).
+* ``online_merge_scores`` / ``online_attention`` -- the blockwise algorithm in
+  the pages' order: per key block, block row max, new running max m_new,
+  alpha = exp(m_old - m_new), p = exp(s - m_new), l = alpha*l + rowsum(p),
+  U = alpha*U + p V, and O = U / l only after the scan (xuesongtap §2.2,
+  equation for U_i^new; operatorworld "在线 softmax：边算边修正" update
+  equations; triton-tutorial §8.3.3).  Used to pin the worked example and the
+  block-split invariance; the GPU path is compared against ``attention``.
+* ``combine`` -- merging partial (U, m, l) triples: m = max_w m_w,
+  l = sum_w exp(m_w - m) l_w, O = sum_w exp(m_w - m) U_w / l (iceferryling
+  "FlashAttention 1 和 FlashAttention 2 的区别", §6 cross-warp merge; the same
+  rule reduces FlashDecoding partials, cnblogs jzssuanfa page, §三 场景 B).
+* ``chunk_partials`` / ``decode`` -- FlashDecoding split-K: one query row, the
+  KV sequence cut into chunks, one partial (U, m, l) per chunk by the plain
+  definition restricted to the chunk (cnblogs §三 场景 B, step 2).
+
+Readings where the pages are silent or disagree (each also listed in the
+design notes):
+* A query row with no admissible key has O = 0 and lse = -inf.
+* When the running max is still -inf, 0 is used as the subtraction base so
+  that alpha and p are 0 instead of NaN (xuesongtap §2.2: "首个非空块的旧贡献
+  系数取 0"; rows that are fully masked skip the invalid exponent difference).
+* U is kept unnormalised and divided by l once at the end (xuesongtap §2.2 and
+  §4; triton-tutorial §8.4.5).  The cnblogs page's block-local normalisation
+  gives the same result.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+the pages print, closed forms, invariants, a library routine and brute force.
+"""
+
+from __future__ import annotations
+
+import itertools
+from typing import Iterable, Sequence
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _f64(x) -> np.ndarray:
+    """Widen any array-like (numpy, torch CPU tensor of bf16/fp32) to fp64."""
+    if hasattr(x, "detach"):  # a torch tensor; bf16 has no numpy dtype
+        x = x.detach().to("cpu").double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def admissible_keys(i: int, n_keys: int, causal: bool) -> np.ndarray:
+    """J(i): the keys query row i may attend to.
+
+    Non-causal: all keys 0..n_keys-1.  Causal (top-left aligned, square):
+    keys 0..i (triton-tutorial §8.7.1: a score survives when row >= column).
+    """
+    hi = min(i + 1, n_keys) if causal else n_keys
+    return np.arange(max(hi, 0))
+
+
+def attention_head(q, k, v, scale: float, causal: bool = False, rows=None):
+    """Plain-definition attention for one (batch, head).
+
+    q: [N, d], k: [Nk, d], v: [Nk, dv]; returns (O [R, dv], lse [R]) for the
+    query rows ``rows`` (default: all N).  One explicit score row per query,
+    the stable softmax of triton-tutorial §8.3.1 (max, exp, sum, divide)
+    applied to S = scale * q k^T (xuesongtap §1; triton-tutorial §8.1).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n = q.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.shape[0], v.shape[1]), dtype=np.float64)
+    lse = np.full(rows.shape[0], NEG_INF, dtype=np.float64)
+    if rows.shape[0] == 0:
+        return out, lse
+    # the explicit N x N score matrix, one row per selected query
+    s_all = float(scale) * (q[rows] @ k.T)
+    for r, i in enumerate(rows):
+        keys = admissible_keys(int(i), k.shape[0], causal)
+        if keys.shape[0] == 0:
+            continue  # reading: no admissible key -> O = 0, lse = -inf
+        s = s_all[r, keys]
+        m = s.max()
+        e = np.exp(s - m)
+        l = e.sum()
+        out[r] = (e @ v[keys]) / l
+        lse[r] = m + np.log(l)
+    return out, lse
+
+
+def attention(q, k, v, scale: float, causal: bool = False, rows=None):
+    """Attention over [B, H, N, d] tensors, head by head.
+
+    ``rows`` selects query rows per head: None (all rows), a 1-D index array
+    (same rows for every head) or a [B, H, R] integer array (rows per head).
+    Returns O [B, H, R, dv] and lse [B, H, R] in fp64.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b_, h_, n = q.shape[0], q.shape[1], q.shape[2]
+    if rows is None:
+        rows_bh = None
+        r = n
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        rows_bh = rows
+        r = rows.shape[-1]
+    out = np.zeros((b_, h_, r, v.shape[-1]))
+    lse = np.zeros((b_, h_, r))
+    for b in range(b_):
+        for h in range(h_):
+            sel = None
+            if rows_bh is not None:
+                sel = rows_bh if rows_bh.ndim == 1 else rows_bh[b, h]
+            out[b, h], lse[b, h] = attention_head(q[b, h], k[b, h], v[b, h], scale, causal, sel)
+    return out, lse
+
+
+def online_merge_scores(score_blocks: Sequence, value_blocks: Sequence, *, rescale_u: bool = True,
+                        trace: list | None = None):
+    """Blockwise online softmax over given score blocks, in the pages' order.
+
+    score_blocks[j]: [R, Bc_j] already-scaled scores (-inf where masked);
+    value_blocks[j]: [Bc_j, dv].  State per row starts at m = -inf, l = 0,
+    U = 0 (xuesongtap §2.2 "初始状态").  For each block (triton-tutorial
+    §8.3.3):
+        m_new = max(m_old, rowmax(S_block))
+        alpha = exp(m_old - m_new)
+        p     = exp(S_block - m_new)
+        l     = alpha * l + rowsum(p)
+        U     = alpha * U + p @ V_block
+    and after the scan O = U / l, lse = m + log(l).
+
+    ``rescale_u=False`` plants the bug the operatorworld page warns about
+    (forgetting to rescale the old output); tests use it to show that the
+    pins catch it.  When ``trace`` is a list, one dict per block with the
+    block's m_new, alpha and l is appended to it.
+    """
+    first = _f64(score_blocks[0])
+    r = first.shape[0]
+    dv = _f64(value_blocks[0]).shape[1]
+    m = np.full(r, NEG_INF)
+    l = np.zeros(r)
+    u = np.zeros((r, dv))
+    for s_blk, v_blk in zip(score_blocks, value_blocks):
+        s_blk = _f64(s_blk)
+        v_blk = _f64(v_blk)
+        if s_blk.shape[1] == 0:
+            continue
+        m_new = np.maximum(m, s_blk.max(axis=1))
+        base = np.where(np.isneginf(m_new), 0.0, m_new)  # fully-masked guard
+        alpha = np.exp(m - base)
+        p = np.exp(s_blk - base[:, None])
+        l = alpha * l + p.sum(axis=1)
+        u = (alpha[:, None] * u if rescale_u else u) + p @ v_blk
+        m = m_new
+        if trace is not None:
+            trace.append({"m_new": m_new.copy(), "alpha": alpha.copy(), "l": l.copy()})
+    safe_l = np.where(l > 0, l, 1.0)
+    o = np.where(l[:, None] > 0, u / safe_l[:, None], 0.0)
+    lse = np.where(l > 0, m + np.log(safe_l), NEG_INF)
+    return o, lse
+
+
+def online_attention_head(q, k, v, scale: float, causal: bool, block_sizes: Iterable[int], *,
+                          rescale_u: bool = True, trace: list | None = None):
+    """One head through the blockwise algorithm with key blocks of the given sizes.
+
+    Q_i stays whole (one query block), the key/value blocks K_j, V_j arrive
+    in order (xuesongtap §2.1; cnblogs §一 inner loop).  Scores of masked
+    pairs are -inf (xuesongtap §2.2, last paragraph).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n = q.shape[0]
+    sizes = list(block_sizes)
+    assert sum(sizes) == k.shape[0], "block sizes must cover the keys"
+    s_blocks, v_blocks = [], []
+    start = 0
+    for bc in sizes:
+        s = float(scale) * (q @ k[start:start + bc].T)
+        if causal:
+            cols = np.arange(start, start + bc)
+            s = np.where(cols[None, :] > np.arange(n)[:, None], NEG_INF, s)
+        s_blocks.append(s)
+        v_blocks.append(v[start:start + bc])
+        start += bc
+    return online_merge_scores(s_blocks, v_blocks, rescale_u=rescale_u, trace=trace)
+
+
+def compositions(n: int):
+    """All ordered ways to cut n keys into consecutive non-empty blocks (2^(n-1))."""
+    for cuts in itertools.product([0, 1], repeat=max(n - 1, 0)):
+        sizes, run = [], 1
+        for c in cuts:
+            if c:
+                sizes.append(run)
+                run = 1
+            else:
+                run += 1
+        sizes.append(run)
+        yield sizes
+
+
+def combine(u_parts, m_parts, l_parts):
+    """Merge partial (U, m, l) triples of the same query rows.
+
+    u_parts [R, S, dv] unnormalised numerators, m_parts [R, S] maxima (natural
+    log units of scaled scores), l_parts [R, S] denominators.  The merge of
+    iceferryling §6: m = max_s m_s, l = sum_s exp(m_s - m) l_s,
+    O = sum_s exp(m_s - m) U_s / l; lse = m + log(l).  An empty partial has
+    m = -inf, l = 0, U = 0 and weight 0; a row whose partials are all empty
+    gets O = 0, lse = -inf.
+    """
+    u, m_p, l_p = _f64(u_parts), _f64(m_parts), _f64(l_parts)
+    m = m_p.max(axis=1)
+    base = np.where(np.isneginf(m), 0.0, m)
+    w = np.exp(m_p - base[:, None])
+    l = (w * l_p).sum(axis=1)
+    num = (w[:, :, None] * u).sum(axis=1)
+    safe_l = np.where(l > 0, l, 1.0)
+    o = np.where(l[:, None] > 0, num / safe_l[:, None], 0.0)
+    lse = np.where(l > 0, m + np.log(safe_l), NEG_INF)
+    return o, lse
+
+
+def chunk_partials(q_row, k, v, scale: float, chunk: int):
+    """FlashDecoding map step for one query row: a partial per KV chunk.
+
+    q_row [d], k/v [L, d]; chunk c covers keys [c*chunk, min(L, (c+1)*chunk)).
+    Each partial is the plain definition restricted to its chunk:
+    m_c = max s, l_c = sum exp(s - m_c), U_c = sum exp(s - m_c) v
+    (cnblogs §三 场景 B step 2: local O_partial with max m and normaliser l).
+    Returns U [C, dv], m [C], l [C].
+    """
+    q_row, k, v = _f64(q_row), _f64(k), _f64(v)
+    n_keys = k.shape[0]
+    n_chunks = -(-n_keys // chunk)
+    u = np.zeros((n_chunks, v.shape[1]))
+    m = np.full(n_chunks, NEG_INF)
+    l = np.zeros(n_chunks)
+    s_all = float(scale) * (k @ q_row)
+    for c in range(n_chunks):
+        s = s_all[c * chunk:(c + 1) * chunk]
+        m[c] = s.max()
+        e = np.exp(s - m[c])
+        l[c] = e.sum()
+        u[c] = e @ v[c * chunk:(c + 1) * chunk]
+    return u, m, l
+
+
+def decode(q, k, v, scale: float, pairs=None):
+    """Single-token decode: q [B, H, d], k/v [B, H, L, d] -> O [P, dv], lse [P].
+
+    The plain definition with one query row and every key admissible.
+    ``pairs`` is an optional [P, 2] array of (b, h) rows to evaluate
+    (default: every (b, h) in order).
+    """
+    b_, h_ = q.shape[0], q.shape[1]
+    if pairs is None:
+        pairs = [(b, h) for b in range(b_) for h in range(h_)]
+    pairs = [(int(b), int(h)) for b, h in pairs]
+    dv = v.shape[-1]
+    out = np.zeros((len(pairs), dv))
+    lse = np.zeros(len(pairs))
+    for idx, (b, h) in enumerate(pairs):
+        o, ls = attention_head(_f64(q[b, h])[None, :], _f64(k[b, h]), _f64(v[b, h]), scale, False)
+        out[idx], lse[idx] = o[0], ls[0]
+    return out, lse

@@ -1,0 +1,494 @@
+"""Benchmark of the attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  The headline workload is the prefill configuration
+(B=4, H=16, N=2048, d=64, non-causal, bf16): one step is one fused forward
+(fa_fwd) over it, timed with CUDA events on the launching stream, L2 flushed
+(256 MiB write) between timed steps because its inputs (50 MB) fit in L2.
+``extra`` carries the other workloads of the target (causal N=8192 d=128 with
+x8 key spikes, ragged causal N=16381, split-KV decode L=32768), each with its
+roofline fraction; their inputs exceed L2.  ``e2e`` repeats the headline
+through the C ABI with pinned host buffers and the host<->device copies
+inside the timed region.  ``cpu_baseline`` is the fp64 oracle timed on the
+host cores over a bounded sample.  ``--impl reference`` times that oracle
+as the reference arm (there is no runnable reference implementation).
+
+Multi-GPU: the work does not shard across GPUs in this design; under torchrun
+every rank runs an independent replica ("scaling": "weak") and the slowest
+rank's time is reported.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "prefill"
+EXTRA = ("causal", "ragged", "decode")
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "attention fwd TFLOPS (bf16, causal/non-causal) and decode GB/s vs GB300 roofline"
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
+# under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
+NCU_TRAFFIC = {
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 927.144e6,
+                               "sha256": "85933a08f7100db1404c7f7b1731b669fb843a68e8573797fdb2f65bf1300dcc"},
+}
+
+
+def _traffic(kernel: str, workload: str):
+    rec = NCU_TRAFFIC.get((kernel, workload))
+    if rec is None:
+        return None
+    try:
+        with open(os.path.join(ROOT, "exact_attention_06_gb300", "csrc", rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+    except OSError:
+        return None
+    return rec["bytes"]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while a region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.device_index = device_index
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        inside = [p for t, p in self.samples if self.t_start and self.t_end and self.t_start <= t <= self.t_end]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [p for _, p in self.samples]
+            window = "warmup+timed"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for p in inside:
+            for name, val in zip(names, p[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def _prefill_step_fn(w, dev, stream):
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+
+    def step():
+        fattn.fa_fwd(q, k, v, o, lse, w.scale, w.causal, stream=stream)
+    return step, 1
+
+
+def _decode_step_fn(w, dev, stream):
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
+    o = torch.empty(w.B, w.H, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(fattn.fa_decode_workspace_bytes(w.B, w.H, w.N, w.d, 128, 0), dtype=torch.uint8, device=dev)
+
+    def step():
+        fattn.fa_decode_splitkv(q, k, v, o, lse, w.scale, ws, 128, 0, stream=stream)
+    return step, 2
+
+
+def _time_steps(step, steps, warmup, stream, flush=None, sampler=None, dist_sync=None):
+    """Per-step CUDA-event times (ms) of exactly `steps` steps after `warmup` untimed ones."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if dist_sync:
+        dist_sync()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t_start")
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            if flush is not None:
+                flush()
+            a.record(stream)
+            step()
+            b.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t_end")
+    if dist_sync:
+        dist_sync()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def _roofline(kind, work_per_launch, launch_ms, peaks, traffic):
+    if kind == "tensor":
+        achieved = work_per_launch / (launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work_per_launch / (launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    return {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peaks['source']} ({'bf16 burst' if kind == 'tensor' else 'copy bandwidth'})"}
+
+
+def _e2e_prefill(w, dev, stream, steps, warmup):
+    """Headline metric through the C ABI from pinned host buffers (copies timed)."""
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    qh, kh, vh = (t.pin_memory() for t in inputs.workload_inputs(w, seed=0, device="cpu"))
+    oh = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(w.B, w.H, w.N, dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+    od = torch.empty_like(qd)
+    ld = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+
+    def step():
+        with torch.cuda.stream(stream):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            fattn.fa_fwd(qd, kd, vd, od, ld, w.scale, w.causal, stream=stream)
+            oh.copy_(od, non_blocking=True)
+            lh.copy_(ld, non_blocking=True)
+
+    ms = _time_steps(step, steps, warmup, stream)
+    t = statistics.mean(ms)
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return {"value": round(w.flops() / (t * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(t, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = _dist()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from exact_attention_06_gb300 import build as _build, inputs
+    if rank == 0 or world == 1:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    peaks = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    def dist_sync():
+        if dist is not None:
+            dist.barrier()
+
+    if args.only:
+        return run_only(args, inputs.WORKLOADS[args.only], dev, stream, peaks, flush)
+    w = inputs.WORKLOADS[HEADLINE]
+    step, launches = _prefill_step_fn(w, dev, stream)
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush, sampler=sampler, dist_sync=dist_sync)
+    sampler.stop()
+    t_local = statistics.mean(ms)
+    t = t_local
+    if dist is not None:
+        tt = torch.tensor([t_local], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    flops = w.flops()
+    value = flops * world / (t * 1e-3) / 1e12
+
+    extra = {}
+    if not args.no_extra:
+        for name in EXTRA:
+            we = inputs.WORKLOADS[name]
+            if we.kind == "decode":
+                st_fn, nl = _decode_step_fn(we, dev, stream)
+            else:
+                st_fn, nl = _prefill_step_fn(we, dev, stream)
+            ems = _time_steps(st_fn, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
+            et = statistics.mean(ems)
+            if we.kind == "decode":
+                work, kind, kern = we.kv_bytes(), "hbm", "decode_split_kernel"
+                val = work / (et * 1e-3) / 1e9
+                unit = "GB/s"
+            else:
+                work, kind, kern = we.flops(), "tensor", "fwd_kernel"
+                val = work / (et * 1e-3) / 1e12
+                unit = "TFLOP/s"
+            extra[name] = {"value": round(val * world, 3), "unit": unit, "ms_per_step": round(et, 4),
+                           "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
+                           "config": {"B": we.B, "H": we.H, "N" if we.kind == "prefill" else "L": we.N, "d": we.d,
+                                      "causal": we.causal, "spike_every_64th_key_x8": we.spike},
+                           "roofline": _roofline(kind, work, et, peaks, _traffic(kern, name)),
+                           "l2": "inputs larger than L2"}
+            if we.kind == "decode":
+                extra[name]["roofline"]["note"] = "duration covers the split kernel and the combine kernel"
+            del st_fn
+            torch.cuda.empty_cache()
+
+    e2e = _e2e_prefill(w, dev, stream, max(3, min(args.steps, 50)), max(3, args.warmup))
+    if world > 1:
+        e2e["value"] = round(e2e["value"] * world, 3)
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w, budget_s=args.cpu_seconds)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1) bf16)",
+        "config": {"workload": "prefill B4 H16 N2048 d64 non-causal", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "scale": w.scale, "global_batch": w.B * world, "seq_len": w.N,
+                   "parallelism": f"replicas x{world}", "l2": "flushed between timed steps (256 MiB write)"},
+        "gpu_launches": launches * args.steps,
+        "roofline": _roofline("tensor", flops, t_local, peaks, _traffic("fwd_kernel", HEADLINE)),
+        "clocks": sampler.summary(),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_only(args, w, dev, stream, peaks, flush):
+    """One workload alone (profiler captures and sweeps): its step timed like the headline."""
+    fn = _decode_step_fn if w.kind == "decode" else _prefill_step_fn
+    step, launches = fn(w, dev, stream)
+    small = w.kind == "prefill" and 3 * w.B * w.H * w.N * w.d * 2 < L2_FLUSH_BYTES
+    ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush if small else None)
+    t = statistics.mean(ms)
+    if w.kind == "decode":
+        work, kind, kern, unit = w.kv_bytes(), "hbm", "decode_split_kernel", "GB/s"
+        value = work / (t * 1e-3) / 1e9
+    else:
+        work, kind, kern, unit = w.flops(), "tensor", "fwd_kernel", "TFLOP/s"
+        value = work / (t * 1e-3) / 1e12
+    print(json.dumps({"workload": w.name, "value": round(value, 3), "unit": unit, "steps": args.steps,
+                      "warmup": args.warmup, "ms_per_step": round(t, 5), "ms_min": round(min(ms), 5),
+                      "gpu_launches": launches * args.steps,
+                      "roofline": _roofline(kind, work, t, peaks, _traffic(kern, w.name))}), flush=True)
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+_CPU_SAMPLE_SCRIPT = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle
+from exact_attention_06_gb300 import inputs
+w = inputs.WORKLOADS[{name!r}]
+steps, per_step, rows_per_call = {steps!r}, {per_step!r}, {rows!r}
+q, k, v = inputs.workload_inputs(w, seed=0, device="cpu")
+out = []
+calls = 0
+for _ in range(steps):
+    done_rows = 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = calls % w.B, (calls // w.B) % w.H
+        rows = inputs.sample_rows(w.N, rows_per_call, seed=calls)
+        oracle.attention_head(q[b, h], k[b, h], v[b, h], w.scale, w.causal, rows=rows.numpy())
+        done_rows += len(rows)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= per_step:
+            break
+    # algorithmic flops of the evaluated rows: 4*d per admissible key (non-causal: all N keys)
+    out.append({{"seconds": el, "rows": done_rows, "flops": done_rows * 4.0 * w.N * w.d}})
+print(json.dumps(out))
+"""
+
+
+def _oracle_steps(w, steps, per_step_s, rows):
+    """Run the fp64 oracle as it stands in a fresh process: `steps` bounded samples of the workload."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    script = _CPU_SAMPLE_SCRIPT.format(root=ROOT, name=w.name, steps=int(steps), per_step=float(per_step_s),
+                                       rows=int(rows))
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, env=env,
+                       timeout=120 + steps * (per_step_s + 30))
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-500:])
+    return json.loads(r.stdout.strip().splitlines()[-1]), cores
+
+
+def cpu_baseline(w, budget_s=12.0, rows=256):
+    """The fp64 oracle on the host cores over a bounded sample (~budget_s seconds) of the workload."""
+    try:
+        res, cores = _oracle_steps(w, 1, budget_s, rows)
+    except (RuntimeError, subprocess.TimeoutExpired) as e:
+        return {"value": None, "unit": "TFLOP/s", "kind": "oracle", "error": str(e)[-300:]}
+    r = res[0]
+    return {"value": round(r["flops"] / r["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{r['rows']} seeded query rows of the {w.name} workload ({rows} rows per call, explicit fp64 "
+                      f"score rows) in {r['seconds']:.1f} s; numpy/BLAS threads={cores}",
+            "seconds": round(r["seconds"], 2)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    from exact_attention_06_gb300 import inputs
+    w = inputs.WORKLOADS[HEADLINE]
+    total = args.steps + args.warmup
+    per_step = max(0.2, min(20.0, args.ref_seconds / total))
+    res, cores = _oracle_steps(w, total, per_step, 64)
+    timed = res[args.warmup:]
+    secs = sum(r["seconds"] for r in timed)
+    flops = sum(r["flops"] for r in timed)
+    value = flops / secs / 1e12
+    line = {
+        "metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000.0 * secs / len(timed), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1) bf16)",
+        "config": {"workload": "prefill B4 H16 N2048 d64 non-causal", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "parallelism": "single process on host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: seeded query rows of the prefill workload for {per_step:.2f} s "
+                                   f"(64 rows per call, explicit fp64 score rows); numpy/BLAS threads={cores}"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--only", default=None, help="time one named workload alone (e.g. causal, decode_small)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

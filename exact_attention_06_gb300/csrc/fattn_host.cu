@@ -1,0 +1,308 @@
+// Host side of the libfattn C ABI: argument validation, TMA tensor-map
+// encoding, kernel launches and the status word.  Declared in fattn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "fattn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+fa_status_t fail(fa_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------- device info
+struct DevInfo {
+  bool known = false;
+  int major = 0, minor = 0, sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+fa_status_t check_device(int* sms) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0) return fail(FA_ERR_ARCH, "no CUDA device: %s", cudaGetErrorString(e));
+  if (dev >= kMaxDevices) return fail(FA_ERR_ARCH, "device ordinal %d out of range", dev);
+  DevInfo info;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_dev[dev].known) {
+      DevInfo d;
+      if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return fail(FA_ERR_ARCH, "cannot query device %d", dev);
+      d.known = true;
+      g_dev[dev] = d;
+    }
+    info = g_dev[dev];
+  }
+  if (info.major != 10 || info.minor != 3)
+    return fail(FA_ERR_ARCH, "device %d has compute capability %d.%d; libfattn is built for sm_103a (10.3)", dev,
+                info.major, info.minor);
+  if (sms) *sms = info.sms;
+  return FA_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A bf16 tensor [batches, rows, d] (d innermost) seen as 3-D {d, rows, batches},
+// loaded in boxes of 64 columns x box_rows rows with 128-byte swizzle.  Rows
+// past `rows` read as zeros.
+fa_status_t make_map(CUtensorMap* map, const void* base, int d, long long rows, long long batches, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batches)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
+  return FA_OK;
+}
+
+constexpr unsigned long long kDefaultBudget = 4000000000ull;  // SM cycles per wait (about 2 s)
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct DecodePlan {
+  int splits = 0;
+  int keys_per_split = 0;
+  size_t u_bytes = 0, m_bytes = 0, l_bytes = 0;
+  size_t total() const { return u_bytes + m_bytes + l_bytes; }
+};
+
+// Splits per (b, h) when the caller passes 0: the fewest that fill the GPU's
+// resident split-CTA slots to within 3% in the last wave (or, when even one
+// partial per chunk cannot fill one wave, one partial per chunk).
+int auto_splits(long long bh, int n_chunks, int sms) {
+  const double slots = static_cast<double>(sms) * fattn::kDecodeCtasPerSm;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= n_chunks; ++s) {
+    const int cps = (n_chunks + s - 1) / s;
+    if ((n_chunks + cps - 1) / cps != s) continue;  // would leave a split empty
+    const double waves = static_cast<double>(bh) * s / slots;
+    const double eff = waves < 1.0 ? waves : waves / std::ceil(waves);
+    if (eff >= 0.97) return s;
+    if (eff > best_eff + 1e-12) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+fa_status_t plan_decode(int B, int H, int L, int d, int chunk, int splits, int sms, DecodePlan* plan) {
+  if (B < 1 || H < 1 || L < 1) return fail(FA_ERR_INVALID_ARG, "B, H and L must be >= 1 (got %d, %d, %d)", B, H, L);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (chunk != 128) return fail(FA_ERR_UNSUPPORTED, "chunk=%d is not supported (128)", chunk);
+  const long long bh = static_cast<long long>(B) * H;
+  const int n_chunks = (L + chunk - 1) / chunk;
+  if (splits < 0 || splits > n_chunks)
+    return fail(FA_ERR_INVALID_ARG, "splits=%d must be in [0, %d] for L=%d", splits, n_chunks, L);
+  const int s = splits == 0 ? auto_splits(bh, n_chunks, sms) : splits;
+  if (bh * s > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H*splits=%lld exceeds the grid limit", bh * s);
+  plan->splits = s;
+  plan->keys_per_split = ((n_chunks + s - 1) / s) * chunk;
+  plan->u_bytes = round256(static_cast<size_t>(bh) * s * d * sizeof(float));
+  plan->m_bytes = round256(static_cast<size_t>(bh) * s * sizeof(float));
+  plan->l_bytes = round256(static_cast<size_t>(bh) * s * sizeof(float));
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status_t status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+const char* fa_last_error(void) { return g_last_error; }
+
+fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                      float scale, int causal, void* stream, const fa_fwd_opts* opts) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H and N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const int o_fp32 = opts ? opts->o_fp32 : 0;
+  if (o_fp32 != 0 && o_fp32 != 1) return fail(FA_ERR_INVALID_ARG, "opts->o_fp32 must be 0 or 1");
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
+  if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 query-tile grid limit", N);
+  fa_status_t st = check_device(nullptr);
+  if (st != FA_OK) return st;
+
+  fattn::FwdLaunch a{};
+  if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tk, k, d, N, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v, d, N, bh, 128)) != FA_OK) return st;
+  a.o = o;
+  a.lse = lse;
+  a.N = N;
+  a.BH = static_cast<int>(bh);
+  a.d = d;
+  a.causal = causal;
+  a.o_fp32 = o_fp32;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
+  cudaGetLastError();  // clear a stale, non-sticky error so that it is not blamed on this launch
+  cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+  return FA_OK;
+}
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, int causal, void* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, stream, nullptr);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int L, int d, int chunk, int splits) {
+  int sms = 0;
+  if (splits == 0) {
+    if (check_device(&sms) != FA_OK) return 0;
+  }
+  DecodePlan plan;
+  if (plan_decode(B, H, L, d, chunk, splits, sms, &plan) != FA_OK) return 0;
+  return plan.total();
+}
+
+fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
+                              int d, float scale, int chunk, int splits, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (workspace && !aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  DecodePlan plan;
+  fa_status_t st;
+  if (splits != 0) {
+    if ((st = plan_decode(B, H, L, d, chunk, splits, 0, &plan)) != FA_OK) return st;
+    if (!workspace || ws_bytes < plan.total())
+      return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes,
+                  plan.total());
+    if ((st = check_device(nullptr)) != FA_OK) return st;
+  } else {
+    int sms = 0;
+    if ((st = plan_decode(B, H, L, d, chunk, 1, 0, &plan)) != FA_OK) return st;  // argument checks first
+    if ((st = check_device(&sms)) != FA_OK) return st;
+    if ((st = plan_decode(B, H, L, d, chunk, 0, sms, &plan)) != FA_OK) return st;
+  }
+  if (!workspace || ws_bytes < plan.total())
+    return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes,
+                plan.total());
+  const long long bh = static_cast<long long>(B) * H;
+  fattn::DecodeLaunch a{};
+  if ((st = make_map(&a.tk, k, d, L, bh, fattn::kDecodeStageKeys)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v, d, L, bh, fattn::kDecodeStageKeys)) != FA_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  a.q = q;
+  a.u_part = reinterpret_cast<float*>(ws);
+  a.m_part = reinterpret_cast<float*>(ws + plan.u_bytes);
+  a.l_part = reinterpret_cast<float*>(ws + plan.u_bytes + plan.m_bytes);
+  a.o = o;
+  a.lse = lse;
+  a.L = L;
+  a.BH = static_cast<int>(bh);
+  a.d = d;
+  a.splits = plan.splits;
+  a.keys_per_split = plan.keys_per_split;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.budget = kDefaultBudget;
+  cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fattn::launch_decode_split(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv split launch");
+  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv combine launch");
+  return FA_OK;
+}
+
+fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
+                       int S, int d, void* stream) {
+  g_last_error[0] = '\0';
+  if (!u_part || !m_part || !l_part || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (R < 1 || S < 1) return fail(FA_ERR_INVALID_ARG, "R and S must be >= 1 (got %d, %d)", R, S);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (!aligned(u_part, 16) || !aligned(o, 16)) return fail(FA_ERR_INVALID_ARG, "u_part and o must be 16-byte aligned");
+  if (!aligned(m_part, 4) || !aligned(l_part, 4) || !aligned(lse, 4))
+    return fail(FA_ERR_INVALID_ARG, "m_part, l_part and lse must be 4-byte aligned");
+  fa_status_t st = check_device(nullptr);
+  if (st != FA_OK) return st;
+  cudaGetLastError();
+  cudaError_t e = fattn::launch_combine(u_part, m_part, l_part, o, lse, R, S, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_combine launch");
+  return FA_OK;
+}
+
+fa_status_t fa_get_status(void* stream) {
+  g_last_error[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_get_status synchronize");
+  const unsigned int bits = fattn::fwd_read_and_clear_status() | fattn::decode_read_and_clear_status();
+  if (bits & fattn::kStatusTimeout) return fail(FA_ERR_TIMEOUT, "a kernel wait exceeded its budget");
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// Internal interface between the C-ABI host code and the kernel translation
+// units.  Not installed; callers use include/fattn.h.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fattn {
+
+// Bits of the per-device status word that kernels raise.
+constexpr unsigned int kStatusTimeout = 1u;
+
+// Forward (prefill) launch description.  The tensor maps describe q, k, v as
+// 3-D tensors {d, N, B*H} (innermost first) with 64 x 128 boxes and 128-byte
+// swizzle.
+struct FwdLaunch {
+  CUtensorMap tq, tk, tv;
+  void* o;
+  float* lse;
+  int N;
+  int BH;
+  int d;
+  int causal;
+  int o_fp32;
+  float scale_log2;  // scale * log2(e)
+  unsigned long long budget;
+};
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+unsigned int fwd_read_and_clear_status();
+
+// Split-KV decode launch description.  The tensor maps describe k, v as 3-D
+// tensors {d, L, B*H} with 64 x kDecodeStageKeys boxes and 128-byte swizzle.
+struct DecodeLaunch {
+  CUtensorMap tk, tv;
+  const void* q;
+  float* u_part;  // [BH, splits, d]
+  float* m_part;  // [BH, splits]
+  float* l_part;  // [BH, splits]
+  void* o;        // [BH, d] bf16
+  float* lse;     // [BH]
+  int L;
+  int BH;
+  int d;
+  int splits;
+  int keys_per_split;  // multiple of 128
+  float scale_log2;
+  unsigned long long budget;
+};
+constexpr int kDecodeStageKeys = 64;  // keys per pipeline stage of the split kernel
+constexpr int kDecodeCtasPerSm = 2;   // resident split CTAs per SM (shared-memory bound)
+cudaError_t launch_decode_split(const DecodeLaunch& a, cudaStream_t stream);
+cudaError_t launch_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse,
+                           int R, int S, int d, cudaStream_t stream);
+unsigned int decode_read_and_clear_status();
+
+}  // namespace fattn

@@ -1,0 +1,144 @@
+"""Thin ctypes binding of the libfattn C ABI (include/fattn.h).
+
+Argument marshalling only: every function takes torch CUDA tensors (or sizes),
+passes their device pointers and the current CUDA stream to the function of
+the same name in ``libfattn.so`` and raises ``FattnError`` on a non-OK status.
+All computation happens in the library's kernels; there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfattn.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_ARCH = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+FA_ERR_WORKSPACE = 6
+
+# Every symbol include/fattn.h declares.
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_decode_workspace_bytes", "fa_decode_splitkv", "fa_combine",
+            "fa_get_status", "fa_status_string", "fa_last_error")
+
+
+class FattnError(RuntimeError):
+    def __init__(self, status: int, func: str, detail: str):
+        self.status = status
+        super().__init__(f"{func}: {status_string(status)}: {detail}")
+
+
+class FaFwdOpts(ctypes.Structure):
+    _fields_ = [("o_fp32", ctypes.c_int), ("wait_budget_cycles", ctypes.c_ulonglong)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FattnError(FA_ERR_CUDA, "load", f"{LIB_PATH} is missing; build it with exact_attention_06_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
+        L.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.fa_decode_workspace_bytes.restype = sz
+        L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+        L.fa_combine.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+        L.fa_get_status.argtypes = [vp]
+        L.fa_status_string.argtypes = [i]
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_last_error.argtypes = []
+        L.fa_last_error.restype = ctypes.c_char_p
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_decode_splitkv", "fa_combine", "fa_get_status"):
+            getattr(L, name).restype = i
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def fa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def fa_last_error() -> str:
+    return lib().fa_last_error().decode()
+
+
+def _check(status: int, func: str):
+    if status != FA_OK:
+        raise FattnError(status, func, fa_last_error())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def fa_fwd_ex(q, k, v, o, lse, scale: float, causal: bool = False, stream=None, o_fp32: bool | None = None,
+              wait_budget_cycles: int = 0):
+    """Fused forward: q, k, v, o [B, H, N, d]; lse [B, H, N] fp32.
+
+    ``o`` may be bf16 (default) or fp32 (``o_fp32``, inferred from o's dtype).
+    """
+    B, H, N, d = q.shape
+    if o_fp32 is None:
+        o_fp32 = o.dtype == torch.float32
+    opts = FaFwdOpts(int(bool(o_fp32)), int(wait_budget_cycles))
+    st = lib().fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
+                         _stream(stream), ctypes.byref(opts))
+    _check(st, "fa_fwd_ex")
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None):
+    """Fused forward with bf16 O (see fa_fwd_ex)."""
+    B, H, N, d = q.shape
+    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
+                      _stream(stream))
+    _check(st, "fa_fwd")
+
+
+def fa_decode_workspace_bytes(B: int, H: int, L: int, d: int, chunk: int = 128, splits: int = 0) -> int:
+    return int(lib().fa_decode_workspace_bytes(B, H, L, d, chunk, splits))
+
+
+def fa_decode_splitkv(q, k, v, o, lse, scale: float, workspace, chunk: int = 128, splits: int = 0, stream=None):
+    """Split-KV decode: q [B, H, d], k/v [B, H, L, d], o [B, H, d], lse [B, H]; workspace a uint8 CUDA tensor."""
+    B, H, L, d = k.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale), chunk,
+                                 splits, _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "fa_decode_splitkv")
+
+
+def fa_combine(u_part, m_part, l_part, o, lse, stream=None):
+    """Merge partials: u_part [R, S, d], m_part/l_part [R, S] fp32 -> o [R, d] bf16, lse [R] fp32."""
+    R, S, d = u_part.shape
+    st = lib().fa_combine(_ptr(u_part), _ptr(m_part), _ptr(l_part), _ptr(o), _ptr(lse), R, S, d, _stream(stream))
+    _check(st, "fa_combine")
+
+
+def fa_get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the kernels' status; raises on a timeout."""
+    st = lib().fa_get_status(_stream(stream))
+    _check(st, "fa_get_status")
+    return st

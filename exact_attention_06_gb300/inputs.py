@@ -56,6 +56,8 @@ WORKLOADS = {
     "causal": Workload("causal", "prefill", 2, 16, 8192, 128, True, spike=True, oracle_rows=512),
     "ragged": Workload("ragged", "prefill", 1, 32, 16381, 128, True, oracle_rows=512),
     "decode": Workload("decode", "decode", 64, 32, 32768, 128, False, oracle_rows=256),
+    # a 2.1 GB slice of the decode workload for profiler captures (still larger than L2)
+    "decode_small": Workload("decode_small", "decode", 4, 32, 32768, 128, False, oracle_rows=16),
 }
 
 

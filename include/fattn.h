@@ -1,0 +1,158 @@
+/*
+ * libfattn -- exact fused attention forward and split-KV decode for GB300
+ * (sm_103a).  C ABI: plain pointers, sizes and a stream handle.
+ *
+ * What is computed (per batch b and head h, scores scaled by `scale`):
+ *     S = scale * Q K^T,   P = softmax(S) row-wise,   O = P V,
+ *     lse_i = m_i + ln(l_i)   (natural log of the scaled scores),
+ * in a single tiled pass with online softmax, so that the N x N score and
+ * probability matrices never reach device memory (xuesongtap.github.io
+ * "flash-attention" page, §1 equation for S, P, O, §2.1 tiling, §2.2 online
+ * softmax, §3 saved log-sum-exp; triton-tutorial "8. FlashAttention 实战",
+ * §8.3.3 incremental formula and §8.4 kernel walk-through).
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers only (memory the caller allocated with the CUDA runtime
+ *     on the current device).  The library allocates nothing, frees nothing
+ *     and keeps no state beyond a cached per-device query (arch, SM count)
+ *     and a per-device status word read by fa_get_status().
+ *   - All tensors are contiguous, row-major in the head dimension d.
+ *   - `stream` is a cudaStream_t (CUstream) handle; NULL is the legacy
+ *     default stream.  Every call is asynchronous on that stream.
+ *   - Arguments are checked before anything is launched; a rejected call
+ *     returns an error status, writes nothing and launches nothing.  No C++
+ *     exception crosses this boundary.  There is no CPU fallback and no
+ *     other backend: an unsupported request is an error.
+ *   - Supported head dimensions: d = 64 and d = 128.
+ *   - Device: compute capability 10.3 (GB300).  Anything else gives
+ *     FA_ERR_ARCH.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, non-finite or non-positive scale */
+  FA_ERR_UNSUPPORTED = 2, /* valid request this library does not implement (e.g. d not in {64, 128}) */
+  FA_ERR_ARCH = 3,        /* current device is not compute capability 10.3, or no device */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+  FA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired; its outputs are undefined */
+  FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than fa_decode_workspace_bytes() */
+} fa_status_t;
+
+/* Options for fa_fwd_ex.  A zero-initialised struct gives fa_fwd's behaviour. */
+typedef struct {
+  int o_fp32;                            /* 0: O is bf16 (round to nearest even); 1: O is fp32 */
+  unsigned long long wait_budget_cycles; /* per-wait spin budget in SM clock cycles; 0 = default (about 2 s) */
+} fa_fwd_opts;
+
+/*
+ * fa_fwd -- fused attention forward (prefill).
+ *
+ * Follows the FA-2 scan order: a 128-row query tile Q_i stays on chip while
+ * the 128-key tiles K_j, V_j stream past it; per tile the running row max m,
+ * the denominator l and the unnormalised output U are updated with
+ * alpha = exp(m_old - m_new), and O = U / l is formed once after the scan
+ * (xuesongtap §2.1-§2.2; triton-tutorial §8.4.1-§8.4.5).
+ *
+ *   q, k, v  [B, H, N, d] bf16, 16-byte aligned.
+ *   o        [B, H, N, d] bf16, 16-byte aligned (written).
+ *   lse      [B, H, N] fp32, 4-byte aligned (written): m + ln(l) of the
+ *            scaled scores, the statistic a backward pass recomputes P from.
+ *   B, H, N  >= 1.   d in {64, 128}.
+ *   scale    finite and > 0 (callers usually pass 1/sqrt(d)).
+ *   causal   0: every key; 1: query i attends keys j <= i (top-left aligned,
+ *            square), masked scores are -inf and tiles above the diagonal
+ *            are skipped (triton-tutorial §8.7.1).
+ * Returns FA_OK once the kernel is queued.  Kernel-side timeouts are reported
+ * by fa_get_status().
+ */
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/* fa_fwd with options (opts may be NULL).  With opts->o_fp32 = 1, `o` is an
+ * fp32 [B, H, N, d] tensor. */
+fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int N, int d, float scale, int causal, void* stream,
+                      const fa_fwd_opts* opts);
+
+/*
+ * fa_decode_workspace_bytes -- bytes of scratch that fa_decode_splitkv needs.
+ *
+ * The workspace holds one partial (U [d] fp32, m fp32, l fp32) per (b, h, split).
+ * `chunk` is the key granularity of a split (must be 128); `splits` is the
+ * number of partials per (b, h), or 0 to let the library choose from L and the
+ * current device's SM count.  Returns 0 for invalid arguments.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int L, int d, int chunk, int splits);
+
+/*
+ * fa_decode_splitkv -- single-token decode with the KV sequence split
+ * (FlashDecoding split-K: the query row is broadcast, each split of the KV
+ * cache yields a partial (O_partial, m, l), and the partials are merged by
+ * the online-softmax rule; cnblogs jzssuanfa page, §三 场景 B; iceferryling
+ * "FlashAttention 1 和 FlashAttention 2 的区别", §13 decode is KV-bandwidth
+ * bound).
+ *
+ *   q        [B, H, d] bf16, 16-byte aligned.
+ *   k, v     [B, H, L, d] bf16, 16-byte aligned (the KV cache, every key
+ *            admissible: no mask).
+ *   o        [B, H, d] bf16 (written).   lse [B, H] fp32 (written).
+ *   L >= 1.  chunk = 128.  splits in [0, ceil(L/128)], 0 = automatic; each
+ *   split covers a whole number of 128-key chunks.  splits = ceil(L/128)
+ *   gives one partial per chunk.
+ *   workspace, ws_bytes: caller-owned device scratch of at least
+ *   fa_decode_workspace_bytes(B, H, L, d, chunk, splits) bytes, 256-byte
+ *   aligned; FA_ERR_WORKSPACE if smaller or NULL.  Its contents on return
+ *   are the partials in fa_combine's layout (u_part, then m_part, then
+ *   l_part, each 256-byte aligned).
+ * Two kernels run on `stream`: the split kernel, then the combine kernel.
+ */
+fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int L, int d, float scale, int chunk, int splits,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * fa_combine -- merge S partial (U, m, l) triples per row into O and lse:
+ *     m = max_s m_s,  w_s = exp(m_s - m),  l = sum_s w_s l_s,
+ *     O = sum_s w_s U_s / l,  lse = m + ln(l)
+ * (iceferryling page §6, cross-warp merge formula; the same rule is the
+ * FlashDecoding tree reduction and the Ring Attention merge).
+ *
+ *   u_part [R, S, d] fp32, unnormalised numerators (relative to exp(s - m_s)).
+ *   m_part [R, S] fp32, row maxima in natural-log units of scaled scores.
+ *   l_part [R, S] fp32, denominators.
+ *   An empty partial (m = -inf, l = 0) has weight 0; a row whose partials are
+ *   all empty gets O = 0 and lse = -inf.
+ *   o [R, d] bf16 (written), lse [R] fp32 (written).  R, S >= 1, d in {64, 128}.
+ *   u_part 16-byte aligned; m_part, l_part, lse 4-byte aligned; o 16-byte aligned.
+ */
+fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part,
+                       void* o, float* lse, int R, int S, int d, void* stream);
+
+/*
+ * fa_get_status -- synchronise `stream`, then read and clear the current
+ * device's kernel status word.  Returns FA_ERR_TIMEOUT if any kernel of this
+ * library ran out of its wait budget since the last call, FA_ERR_CUDA if the
+ * synchronisation itself failed, else FA_OK.
+ */
+fa_status_t fa_get_status(void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa_status_string(fa_status_t status);
+
+/* Detail of the most recent error on the calling thread (static thread-local
+ * storage, "" if none). */
+const char* fa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and rejects
+bad arguments on the host before touching a GPU (no compute calls here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from _util import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "fattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    from exact_attention_06_gb300 import fattn
+    return fattn.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("fa_fwd", "fa_fwd_ex", "fa_decode_splitkv", "fa_decode_workspace_bytes", "fa_combine",
+              "fa_get_status", "fa_status_string", "fa_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from exact_attention_06_gb300 import fattn
+    names = _declared_functions()
+    assert sorted(fattn.EXPORTED) == names
+    for n in names:
+        assert hasattr(lib, n), f"libfattn.so does not export {n}"
+
+
+def test_status_strings(lib):
+    from exact_attention_06_gb300 import fattn
+    assert fattn.status_string(0) == "FA_OK"
+    assert fattn.status_string(fattn.FA_ERR_TIMEOUT) == "FA_ERR_TIMEOUT"
+    assert fattn.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def _fwd(lib, ptrs=(16, 16, 16, 16, 16), B=1, H=1, N=8, d=64, scale=0.125, causal=0):
+    vp = ctypes.c_void_p
+    return lib.fa_fwd(vp(ptrs[0]), vp(ptrs[1]), vp(ptrs[2]), vp(ptrs[3]), vp(ptrs[4]), B, H, N, d,
+                      ctypes.c_float(scale), causal, vp(0))
+
+
+def test_forward_argument_checks_need_no_gpu(lib):
+    from exact_attention_06_gb300 import fattn
+    assert _fwd(lib, ptrs=(0, 16, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG
+    assert _fwd(lib, N=0) == fattn.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=-1) == fattn.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96) == fattn.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, scale=float("nan")) == fattn.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == fattn.FA_ERR_INVALID_ARG
+    assert _fwd(lib, causal=2) == fattn.FA_ERR_INVALID_ARG
+    assert _fwd(lib, ptrs=(16, 24, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # misaligned k
+    assert _fwd(lib, ptrs=(16, 16, 16, 16, 18)) == fattn.FA_ERR_INVALID_ARG  # misaligned lse
+    assert _fwd(lib, N=65535 * 128 + 1) == fattn.FA_ERR_UNSUPPORTED
+    assert "aligned" in fattn.fa_last_error() or "N=" in fattn.fa_last_error()
+
+
+def test_decode_workspace_sizes(lib):
+    from exact_attention_06_gb300 import fattn
+    # explicit splits need no device: R*S*d floats + R*S + R*S floats, each rounded up to 256 bytes
+    assert fattn.fa_decode_workspace_bytes(64, 32, 32768, 128, 128, 4) == 2048 * 4 * 128 * 4 + 2 * 2048 * 4 * 4
+    assert fattn.fa_decode_workspace_bytes(1, 1, 1, 64, 128, 1) == 256 * 3
+    assert fattn.fa_decode_workspace_bytes(1, 1, 1000, 64, 128, 9) == 0  # more splits than 128-key chunks
+    assert fattn.fa_decode_workspace_bytes(1, 1, 1000, 64, 64, 1) == 0   # chunk must be 128
+    assert fattn.fa_decode_workspace_bytes(1, 1, 1000, 80, 128, 1) == 0
+    assert fattn.fa_decode_workspace_bytes(1, 1, 0, 64, 128, 1) == 0
+
+
+def test_decode_and_combine_argument_checks_need_no_gpu(lib):
+    from exact_attention_06_gb300 import fattn
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    st = lib.fa_decode_splitkv(vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, 256, 128, f(0.1), 128, 1, vp(256),
+                               ctypes.c_size_t(16), vp(0))
+    assert st == fattn.FA_ERR_WORKSPACE
+    st = lib.fa_decode_splitkv(vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, 256, 128, f(0.1), 128, 3, vp(256),
+                               ctypes.c_size_t(1 << 20), vp(0))
+    assert st == fattn.FA_ERR_INVALID_ARG  # 3 splits > 2 chunks
+    st = lib.fa_decode_splitkv(vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, 256, 128, f(0.1), 128, 1, vp(264),
+                               ctypes.c_size_t(1 << 20), vp(0))
+    assert st == fattn.FA_ERR_INVALID_ARG  # workspace not 256-byte aligned
+    st = lib.fa_combine(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 0, 128, vp(0))
+    assert st == fattn.FA_ERR_INVALID_ARG
+    st = lib.fa_combine(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 2, 32, vp(0))
+    assert st == fattn.FA_ERR_UNSUPPORTED

@@ -22,6 +22,8 @@
 // memory at the end with the same rule as the combine kernel.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -313,6 +315,33 @@ cudaError_t launch_combine(const float* u_part, const float* m_part, const float
     combine_kernel<128><<<static_cast<unsigned>(R), 128, 0, stream>>>(u_part, m_part, l_part,
                                                                        static_cast<__nv_bfloat16*>(o), lse, S);
   return cudaGetLastError();
+}
+
+// Scratch for fa_decode_splitkv_noalloc: the per-split partials live here
+// instead of in a caller-provided workspace.  It is a file-scope device array,
+// so every GPU that loads this code keeps kNoAllocScratchBytes of it until the
+// process exits.  In host code `g_noalloc_scratch` only names a host-side
+// stand-in; its device address comes from cudaGetSymbolAddress, once per
+// device, with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t decode_noalloc_scratch(void** ptr) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 unsigned int decode_read_and_clear_status() {

@@ -279,6 +279,34 @@ fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void*
   return FA_OK;
 }
 
+fa_status_t fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                      int L, int d, float scale, int chunk, int splits, void* stream) {
+  g_last_error[0] = '\0';
+  // Size the partials exactly as fa_decode_splitkv would, and refuse what the
+  // fixed scratch cannot hold (argument errors are reported as such first).
+  DecodePlan plan;
+  fa_status_t st;
+  if (splits != 0) {
+    if ((st = plan_decode(B, H, L, d, chunk, splits, 0, &plan)) != FA_OK) return st;
+  } else {
+    int sms = 0;
+    if ((st = plan_decode(B, H, L, d, chunk, 1, 0, &plan)) != FA_OK) return st;
+    if ((st = check_device(&sms)) != FA_OK) return st;
+    if ((st = plan_decode(B, H, L, d, chunk, 0, sms, &plan)) != FA_OK) return st;
+  }
+  if (plan.total() > fattn::kNoAllocScratchBytes)
+    return fail(FA_ERR_WORKSPACE,
+                "fa_decode_splitkv_noalloc: B=%d H=%d with %d splits needs %zu bytes of partials, more than its "
+                "fixed scratch of %zu bytes; use fewer splits or fa_decode_splitkv with a workspace",
+                B, H, plan.splits, plan.total(), fattn::kNoAllocScratchBytes);
+  if ((st = check_device(nullptr)) != FA_OK) return st;
+  void* scratch = nullptr;
+  cudaError_t e = fattn::decode_noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_noalloc scratch address");
+  return fa_decode_splitkv(q, k, v, o, lse, B, H, L, d, scale, chunk, plan.splits, scratch,
+                           fattn::kNoAllocScratchBytes, stream);
+}
+
 fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
                        int S, int d, void* stream) {
   g_last_error[0] = '\0';

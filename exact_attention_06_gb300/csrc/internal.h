@@ -54,4 +54,10 @@ cudaError_t launch_combine(const float* u_part, const float* m_part, const float
                            int R, int S, int d, cudaStream_t stream);
 unsigned int decode_read_and_clear_status();
 
+// Fixed device scratch used by fa_decode_splitkv_noalloc in place of a
+// caller-provided workspace.  Size limit of that entry point.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t decode_noalloc_scratch(void** ptr);
+
 }  // namespace fattn

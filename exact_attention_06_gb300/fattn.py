@@ -25,8 +25,9 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_decode_workspace_bytes", "fa_decode_splitkv", "fa_combine",
-            "fa_get_status", "fa_status_string", "fa_last_error")
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_decode_workspace_bytes", "fa_decode_splitkv", "fa_decode_splitkv_noalloc",
+            "fa_combine", "fa_get_status", "fa_status_string", "fa_last_error")
+FA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class FattnError(RuntimeError):
@@ -55,13 +56,15 @@ def lib() -> ctypes.CDLL:
         L.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.fa_decode_workspace_bytes.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+        L.fa_decode_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         L.fa_combine.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
         L.fa_get_status.argtypes = [vp]
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_decode_splitkv", "fa_combine", "fa_get_status"):
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_combine",
+                     "fa_get_status"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -128,6 +131,19 @@ def fa_decode_splitkv(q, k, v, o, lse, scale: float, workspace, chunk: int = 128
     st = lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale), chunk,
                                  splits, _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "fa_decode_splitkv")
+
+
+def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, chunk: int = 128, splits: int = 0, stream=None):
+    """fa_decode_splitkv without a workspace, for callers that cannot allocate device memory.
+
+    The partials go to a fixed 8 MiB device array inside the library; larger
+    requests raise FattnError(FA_ERR_WORKSPACE).  Calls that overlap on the GPU
+    share that array and race: keep them on one stream.
+    """
+    B, H, L, d = k.shape
+    st = lib().fa_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale),
+                                         chunk, splits, _stream(stream))
+    _check(st, "fa_decode_splitkv_noalloc")
 
 
 def fa_combine(u_part, m_part, l_part, o, lse, stream=None):

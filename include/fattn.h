@@ -14,8 +14,9 @@
  * Conventions shared by every entry point
  *   - Device pointers only (memory the caller allocated with the CUDA runtime
  *     on the current device).  The library allocates nothing, frees nothing
- *     and keeps no state beyond a cached per-device query (arch, SM count)
- *     and a per-device status word read by fa_get_status().
+ *     and keeps no state beyond a cached per-device query (arch, SM count),
+ *     a per-device status word read by fa_get_status() and the fixed scratch
+ *     array of fa_decode_splitkv_noalloc.
  *   - All tensors are contiguous, row-major in the head dimension d.
  *   - `stream` is a cudaStream_t (CUstream) handle; NULL is the legacy
  *     default stream.  Every call is asynchronous on that stream.
@@ -117,6 +118,41 @@ size_t fa_decode_workspace_bytes(int B, int H, int L, int d, int chunk, int spli
 fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H, int L, int d, float scale, int chunk, int splits,
                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * fa_decode_splitkv_noalloc -- fa_decode_splitkv for callers that cannot
+ * allocate device memory.  (The pages have no counterpart to this entry
+ * point: it exists for embedding, not for the method.)
+ *
+ * Some callers are handed only their input and output buffers and may not
+ * call cudaMalloc themselves: plugins inside inference runtimes that own all
+ * device memory through their own allocator, and request paths that must not
+ * pay for, or risk the device-wide synchronisation of, an allocation or a
+ * free.  They have no workspace to pass, so this entry point keeps the
+ * per-split partials in a fixed array of device memory compiled into the
+ * library (FA_NOALLOC_SCRATCH_BYTES, 8 MiB) instead.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *   Arguments as fa_decode_splitkv, without workspace and ws_bytes.
+ *   The partials of B*H rows with S splits take
+ *   fa_decode_workspace_bytes(B, H, L, d, chunk, S) bytes; a request larger
+ *   than FA_NOALLOC_SCRATCH_BYTES returns FA_ERR_WORKSPACE (fa_last_error()
+ *   says by how much) and launches nothing.  B*H*S*(d+2)*4 bytes is about the
+ *   need: e.g. B*H = 2048 rows at d = 128 fit up to 7 splits.
+ *   Every GPU that loads the library's decode code holds the 8 MiB array until
+ *   the process exits.  The first call on each device looks up the array's
+ *   device address (cudaGetSymbolAddress) with that device current; make that
+ *   first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's partials:
+ *   nothing in it needs to start at zero (every partial is written before it
+ *   is read), but calls whose kernels overlap on the GPU -- on different
+ *   streams, or from different host threads -- race on it and give undefined
+ *   results.  Serialise them (one stream, or events).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+fa_status_t fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                      int B, int H, int L, int d, float scale, int chunk, int splits,
+                                      void* stream);
 
 /*
  * fa_combine -- merge S partial (U, m, l) triples per row into O and lse:

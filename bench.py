@@ -61,6 +61,13 @@ def _peaks():
 NCU_TRAFFIC = {
     ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 927.144e6,
                                "sha256": "85933a08f7100db1404c7f7b1731b669fb843a68e8573797fdb2f65bf1300dcc"},
+    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.673e6,
+                                "sha256": "85933a08f7100db1404c7f7b1731b669fb843a68e8573797fdb2f65bf1300dcc"},
+    # captured on the B4 slice, scaled x16 to the B64 decode workload (one read of each row's K/V)
+    ("decode_split_kernel", "decode"): {"source": "fa_decode.cu", "bytes": 2151.209e6 * 16,
+                                        "sha256": "998d073e4a431723d2d4c2ee2e3b37b318d91d376f6e1c258655d2d7986f2ab9"},
+    ("decode_split_kernel", "decode_small"): {"source": "fa_decode.cu", "bytes": 2151.209e6,
+                                              "sha256": "998d073e4a431723d2d4c2ee2e3b37b318d91d376f6e1c258655d2d7986f2ab9"},
 }
 
 

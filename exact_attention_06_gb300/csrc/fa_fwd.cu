@@ -1,30 +1,37 @@
 // Fused exact attention forward (prefill) for sm_103a.
 //
-// One CTA owns one 128-row query tile Q_i of one (batch, head) and scans the
-// 128-key tiles K_j, V_j once, FA-2 order (xuesongtap.github.io
-// "flash-attention" page, §2.1; triton-tutorial "8. FlashAttention 实战",
-// §8.4.1: Q outer and resident, K/V inner and streamed).  Per tile:
-//   S_ij = Q_i K_j^T                   tcgen05.mma, bf16 x bf16 -> fp32 in TMEM
-//   m_new = max(m, rowmax(S) * c)      c = scale * log2(e)  (exp2 trick, §8.7.3)
-//   alpha = 2^(m - m_new),  P~ = 2^(S*c - m_new)  (online softmax, §8.3.3)
+// One CTA owns two 128-row query tiles Q_0, Q_1 (rows 256p .. 256p+255) of one
+// (batch, head) and scans the 128-key tiles K_j, V_j once, FA-2 order
+// (xuesongtap.github.io "flash-attention" page, §2.1; triton-tutorial
+// "8. FlashAttention 实战", §8.4.1: Q outer and resident, K/V inner and
+// streamed).  Per tile and query tile t:
+//   S_t = Q_t K_j^T                    tcgen05.mma, bf16 x bf16 -> fp32 in TMEM
+//   m_new = max(m, rowmax(S_t) * c)    c = scale * log2(e)  (exp2 trick, §8.7.3)
+//   alpha = 2^(m - m_new),  P~ = 2^(S_t*c - m_new)  (online softmax, §8.3.3)
 //   l = alpha * l + rowsum(P~)         fp32, from the unrounded P~
-//   U = alpha * U + bf16(P~) V_j       P~ written back to TMEM as the A operand
+//   U_t = alpha * U_t + bf16(P~) V_j   P~ written back to TMEM as the A operand
 // and after the scan O = U / l, lse = (m + log2 l) * ln 2.
 //
-// Warp roles (FA-3 style producer/consumer split, triton-tutorial §8.10.2,
-// re-done with Blackwell's TMA + tcgen05 + TMEM):
-//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t),
+// Warp roles (the producer/consumer split and the two-consumer "ping-pong" of
+// triton-tutorial §8.10.2-§8.10.3, re-done with TMA + tcgen05 + TMEM):
+//   warps 0-3  softmax of Q_0: thread r owns row r of the tile (TMEM lane r),
 //              so no cross-thread row reduction is needed (iceferryling
-//              "FlashAttention 1 和 FlashAttention 2 的区别", §7-8 split-Q);
-//              they also apply the alpha rescale of U and the epilogue.
-//   warp 4     TMA producer: Q once, then K_j / V_j into an ST-stage ring.
-//   warp 5     MMA issuer (one thread) and TMEM owner.
-// TMEM columns: S/P double buffer at 0 and 128 (P~ as packed bf16 in the
-// first 64 columns of its S buffer), U at 256..256+d.
+//              "FlashAttention 1 和 FlashAttention 2 的区别", §7-8 split-Q); it
+//              also applies the alpha rescale of U_0 and writes O_0, lse.
+//   warps 4-7  the same for Q_1.
+//   warp 8     MMA issuer (one thread) and TMEM owner.
+//   warp 9     TMA producer: Q_0, Q_1 once, then K_j and V_j into two rings.
+// The tensor core alternates between the tiles: [PV_0(j-1), S_0(j)] runs while
+// the Q_1 softmax works on S_1(j-1), and [PV_1(j-1), S_1(j)] while the Q_0
+// softmax works on S_0(j).  The commit after S_t(j) also covers PV_t(j-1), so
+// the softmax that sees S_t(j) may rescale U_t in place.
+// TMEM columns: S_0/P~_0 at 0, S_1/P~_1 at 128 (P~ as packed bf16 in the first
+// 64 columns of its S), U_0 at 256, U_1 at 256 + d.
 //
-// Causal: key tiles above the diagonal are never loaded; only the diagonal
-// tile masks (col > row -> -inf), and the ragged last tile masks col >= N
-// (triton-tutorial §8.7.1 STAGE split; xuesongtap §2.2 last paragraph).
+// Causal: key tiles above a query tile's diagonal are never computed for it
+// (Q_0 stops one tile before Q_1); only the diagonal tile masks (col > row ->
+// -inf), and the ragged last tile masks col >= N (triton-tutorial §8.7.1
+// STAGE split; xuesongtap §2.2 last paragraph).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -39,27 +46,31 @@ namespace {
 
 constexpr int kBr = 128;                 // query rows per tile (TMEM lanes, MMA M)
 constexpr int kBc = 128;                 // keys per tile
+constexpr int kRowsPerCta = 2 * kBr;
 constexpr uint32_t kBox = 128u * 128u;   // bytes of a 128-row x 64-column bf16 box
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kWarpMma = 8, kWarpTma = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NH = D / 64;                // 64-column boxes per row
-  static constexpr int ST = (D == 128) ? 2 : 4;    // K/V ring stages
-  static constexpr uint32_t QB = NH * kBox;        // bytes of the Q tile
-  static constexpr uint32_t KVB = NH * kBox;       // bytes of one K (or V) tile
-  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + ST, B_EMPTY = B_VF + ST, B_SF = B_EMPTY + ST,
-                       B_PF = B_SF + 2, B_OD = B_PF + 2, B_DRAIN = B_OD + 1, NBAR = B_DRAIN + 1;
+  static constexpr int NH = D / 64;                 // 64-column boxes per row
+  static constexpr int KST = (D == 128) ? 3 : 4;    // K ring stages
+  static constexpr int VST = (D == 128) ? 2 : 4;    // V ring stages
+  static constexpr uint32_t QB = NH * kBox;         // bytes of one Q tile
+  static constexpr uint32_t KVB = NH * kBox;        // bytes of one K (or V) tile
+  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
+                       B_SF = B_VE + VST, B_PF = B_SF + 2, B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = QB;
-  static constexpr uint32_t OFF_V = OFF_K + ST * KVB;
-  static constexpr uint32_t OFF_BAR = OFF_V + ST * KVB;
+  static constexpr uint32_t OFF_K = 2 * QB;
+  static constexpr uint32_t OFF_V = OFF_K + KST * KVB;
+  static constexpr uint32_t OFF_BAR = OFF_V + VST * KVB;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;  // TMEM address slot, abort flag
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;   // + slack to align the base to 1 KB
 };
+static_assert(FwdCfg<128>::SMEM <= 232448, "shared memory of the d=128 kernel exceeds 227 KB");
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long budget) {
@@ -79,19 +90,56 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
   }
 }
 
+// U_t row *= alpha, 32 columns at a time.
 template <int D>
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[D]);
-template <>
-__device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld_x64(taddr, r); }
-template <>
-__device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, uint32_t (&r)[128]) { tmem_ld_x128(taddr, r); }
+__device__ __forceinline__ void rescale_row(uint32_t taddr, float alpha) {
+  const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t ur[32];
+    tmem_ld_x32(taddr + 32 * c, ur);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1])), a2), lo, hi);
+      ur[2 * i] = __float_as_uint(lo);
+      ur[2 * i + 1] = __float_as_uint(hi);
+    }
+    tmem_st_x32(taddr + 32 * c, ur);
+  }
+}
+
+// O row = U row / l to global memory, lse.  Every lane of the warp runs the
+// TMEM loads (tcgen05.ld is warp-collective); only rows < N are stored.
 template <int D>
-__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[D]);
-template <>
-__device__ __forceinline__ void tmem_st_row<64>(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st_x64(taddr, r); }
-template <>
-__device__ __forceinline__ void tmem_st_row<128>(uint32_t taddr, const uint32_t (&r)[128]) {
-  tmem_st_x128(taddr, r);
+__device__ __forceinline__ void store_row(void* o, float* lse, size_t row_off, bool valid, bool o_fp32,
+                                          uint32_t taddr, float l, float m2) {
+  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t ur[32];
+    tmem_ld_x32(taddr + 32 * c, ur);
+    if (!valid) continue;
+    if (o_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + row_off * D + 32 * c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(ur[4 * i]) * inv, __uint_as_float(ur[4 * i + 1]) * inv,
+                             __uint_as_float(ur[4 * i + 2]) * inv, __uint_as_float(ur[4 * i + 3]) * inv);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + row_off * D + 32 * c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(ur[8 * i + 0]) * inv, __uint_as_float(ur[8 * i + 1]) * inv);
+        w.y = pack_bf16(__uint_as_float(ur[8 * i + 2]) * inv, __uint_as_float(ur[8 * i + 3]) * inv);
+        w.z = pack_bf16(__uint_as_float(ur[8 * i + 4]) * inv, __uint_as_float(ur[8 * i + 5]) * inv);
+        w.w = pack_bf16(__uint_as_float(ur[8 * i + 6]) * inv, __uint_as_float(ur[8 * i + 7]) * inv);
+        dst[i] = w;
+      }
+    }
+  }
+  if (valid) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
 }
 
 template <int D, bool CAUSAL>
@@ -112,27 +160,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
-  const int qt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest causal tiles first
+  const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest causal work first
   const int n_tiles = (N + kBc - 1) / kBc;
-  const int n_kv = CAUSAL ? min(qt + 1, n_tiles) : n_tiles;
+  // KV steps of each query tile: all key tiles, or (causal) those up to its diagonal; 0 if the tile is past N.
+  auto steps_of = [&](int t) {
+    const int row0 = pair * kRowsPerCta + t * kBr;
+    return row0 >= N ? 0 : (CAUSAL ? min(row0 / kBc + 1, n_tiles) : n_tiles);
+  };
+  const int n_t0 = steps_of(0), n_t1 = steps_of(1);
+  const int n_max = max(n_t0, n_t1);
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
-    for (int s = 0; s < C::ST; ++s) {
+    for (int s = 0; s < C::KST; ++s) {
       mbar_init(BAR(C::B_KF + s), 1);
+      mbar_init(BAR(C::B_KE + s), 1);
+    }
+    for (int s = 0; s < C::VST; ++s) {
       mbar_init(BAR(C::B_VF + s), 1);
-      mbar_init(BAR(C::B_EMPTY + s), 1);
+      mbar_init(BAR(C::B_VE + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(BAR(C::B_SF + b), 1);
-      mbar_init(BAR(C::B_PF + b), kBr);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(C::B_SF + t), 1);
+      mbar_init(BAR(C::B_PF + t), kBr);
     }
-    mbar_init(BAR(C::B_OD), 1);
     mbar_init(BAR(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -141,177 +197,202 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(BAR(C::B_Q), C::QB);
-      for (int h = 0; h < C::NH; ++h) tma_load_3d(sQ + h * kBox, &tq, BAR(C::B_Q), h * 64, qt * kBr, bh);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % C::ST;
-        if (j >= C::ST &&
-            !mbar_wait(BAR(C::B_EMPTY + s), ((j / C::ST) - 1) & 1, abort_flag, budget, &g_fwd_status))
+      mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QB);
+      for (int t = 0; t < 2; ++t)
+        for (int h = 0; h < C::NH; ++h)
+          tma_load_3d(sQ + t * C::QB + h * kBox, &tq, BAR(C::B_Q), h * 64, pair * kRowsPerCta + t * kBr, bh);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n_max; ++j) {
+        const int ks = j % C::KST;
+        if (j >= C::KST &&
+            !mbar_wait(BAR(C::B_KE + ks), ((j / C::KST) - 1) & 1, abort_flag, budget, &g_fwd_status))
           break;
-        mbar_arrive_expect_tx(BAR(C::B_KF + s), C::KVB);
+        mbar_arrive_expect_tx(BAR(C::B_KF + ks), C::KVB);
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sK + s * C::KVB + h * kBox, &tk, BAR(C::B_KF + s), h * 64, j * kBc, bh);
-        mbar_arrive_expect_tx(BAR(C::B_VF + s), C::KVB);
+          tma_load_3d(sK + ks * C::KVB + h * kBox, &tk, BAR(C::B_KF + ks), h * 64, j * kBc, bh);
+        k_issued = j + 1;
+        const int vs = j % C::VST;
+        if (j >= C::VST &&
+            !mbar_wait(BAR(C::B_VE + vs), ((j / C::VST) - 1) & 1, abort_flag, budget, &g_fwd_status))
+          break;
+        mbar_arrive_expect_tx(BAR(C::B_VF + vs), C::KVB);
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sV + s * C::KVB + h * kBox, &tv, BAR(C::B_VF + s), h * 64, j * kBc, bh);
-        issued = j + 1;
+          tma_load_3d(sV + vs * C::KVB + h * kBox, &tv, BAR(C::B_VF + vs), h * 64, j * kBc, bh);
+        v_issued = j + 1;
       }
       // Every copy this CTA started must land before its shared memory is released.
       drain_wait(BAR(C::B_Q), 0, budget);
-      for (int j = issued - C::ST < 0 ? 0 : issued - C::ST; j < issued; ++j) {
-        drain_wait(BAR(C::B_KF + j % C::ST), (j / C::ST) & 1, budget);
-        drain_wait(BAR(C::B_VF + j % C::ST), (j / C::ST) & 1, budget);
-      }
+      for (int j = max(0, k_issued - C::KST); j < k_issued; ++j)
+        drain_wait(BAR(C::B_KF + j % C::KST), (j / C::KST) & 1, budget);
+      for (int j = max(0, v_issued - C::VST); j < v_issued; ++j)
+        drain_wait(BAR(C::B_VF + j % C::VST), (j / C::VST) & 1, budget);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);  // S = Q K^T, both K-major
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);    // U += P V, V is MN-major
-      bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, budget, &g_fwd_status);
-      tc_fence_after();
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % C::ST;
-        if (!mbar_wait(BAR(C::B_KF + s), (j / C::ST) & 1, abort_flag, budget, &g_fwd_status)) return false;
-        tc_fence_after();
-        const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qb = sQ + t * C::QB;
+        const uint32_t kb = sK + (j % C::KST) * C::KVB;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
-          mma_ss(d_s, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + s * C::KVB + off, 16, 1024), idesc_s,
+          mma_ss(tmem + t * kBc, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_s,
                  kk > 0 ? 1u : 0u);
         }
-        tc_commit(BAR(C::B_SF + (j & 1)));
-        return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(BAR(C::B_PF + (j & 1)), (j >> 1) & 1, abort_flag, budget, &g_fwd_status)) break;
-        const int s = j % C::ST;
-        if (!mbar_wait(BAR(C::B_VF + s), (j / C::ST) & 1, abort_flag, budget, &g_fwd_status)) break;
-        tc_fence_after();
-        const uint32_t a_p = tmem + ((j & 1) ? kColS1 : kColS0);
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = sV + (j % C::VST) * C::KVB;
 #pragma unroll
         for (int kk = 0; kk < kBc / 16; ++kk) {
           // 16 keys per MMA: 16 rows x 128 B of each 64-column V box; boxes kBox apart along d.
-          const uint64_t b_desc = sdesc_sw128(sV + s * C::KVB + static_cast<uint32_t>(kk) * 2048u, kBox, 1024);
-          mma_ts(tmem + kColO, a_p + static_cast<uint32_t>(kk) * 8u, b_desc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kColO + t * D, tmem + t * kBc + static_cast<uint32_t>(kk) * 8u,
+                 sdesc_sw128(vb + static_cast<uint32_t>(kk) * 2048u, kBox, 1024), idesc_o,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(BAR(C::B_OD));
-        tc_commit(BAR(C::B_EMPTY + s));
+      };
+      bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, budget, &g_fwd_status) &&
+                mbar_wait(BAR(C::B_KF), 0, abort_flag, budget, &g_fwd_status);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if ((t ? n_t1 : n_t0) > 0) {
+            issue_s(t, 0);
+            tc_commit(BAR(C::B_SF + t));
+          }
+        tc_commit(BAR(C::B_KE));
+      }
+      for (int j = 1; ok && j <= n_max; ++j) {
+        bool v_ready = false, k_ready = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nt = t ? n_t1 : n_t0;
+          if (!ok || j - 1 >= nt) continue;
+          if (!mbar_wait(BAR(C::B_PF + t), (j - 1) & 1, abort_flag, budget, &g_fwd_status)) {
+            ok = false;
+            break;
+          }
+          if (!v_ready) {
+            const int vs = (j - 1) % C::VST;
+            if (!mbar_wait(BAR(C::B_VF + vs), ((j - 1) / C::VST) & 1, abort_flag, budget, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            v_ready = true;
+          }
+          tc_fence_after();
+          issue_pv(t, j - 1);
+          if (j < nt) {
+            if (!k_ready) {
+              const int ks = j % C::KST;
+              if (!mbar_wait(BAR(C::B_KF + ks), (j / C::KST) & 1, abort_flag, budget, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              k_ready = true;
+              tc_fence_after();
+            }
+            issue_s(t, j);
+          }
+          tc_commit(BAR(C::B_SF + t));  // S_t(j) ready, and PV_t(j-1) done: U_t may be rescaled
+        }
+        if (!ok) break;
+        tc_commit(BAR(C::B_VE + (j - 1) % C::VST));
+        if (j < n_max) tc_commit(BAR(C::B_KE + j % C::KST));
       }
       // All MMAs must be complete before TMEM is released.
       tc_commit(BAR(C::B_DRAIN));
       drain_wait(BAR(C::B_DRAIN), 0, budget);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 0-3
-    const int t = threadIdx.x;  // TMEM lane = row within the tile
-    const int row = qt * kBr + t;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax warps 0-7
+    const int t = warp >> 2;                      // query tile of this warpgroup
+    const int r = threadIdx.x - t * kBr;          // TMEM lane = row within the tile
+    const int row = pair * kRowsPerCta + t * kBr + r;
+    const int n = t ? n_t1 : n_t0;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + static_cast<uint32_t>(t * kBc);
+    const uint32_t t_o = tmem + lane_addr + kColO + static_cast<uint32_t>(t * D);
     const int lim = CAUSAL ? min(row, N - 1) : N - 1;  // last admissible key of this row
+    const uint64_t c2 = f2_pack(sl2, sl2);
     float m2 = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      const uint32_t col_s = b ? kColS1 : kColS0;
-      ok = wait_all(BAR(C::B_SF + b), (j >> 1) & 1, abort_flag, budget);
+    bool ok = n > 0;
+    for (int j = 0; ok && j < n; ++j) {
+      ok = wait_all(BAR(C::B_SF + t), j & 1, abort_flag, budget);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[128];
-      tmem_ld_x128(tmem + lane_addr + col_s, sr);
+      tmem_ld_x128(t_s, sr);
       const int nvalid = lim - j * kBc + 1;  // admissible keys of this tile for this row
       if (nvalid < kBc) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
       }
-      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+      float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
+      float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[i]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[i + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[i + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[i + 3]));
+      for (int i = 4; i < 124; i += 8) {
+        a0 = fmax3(a0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+        a1 = fmax3(a1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+        a2 = fmax3(a2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+        a3 = fmax3(a3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      a0 = fmax3(a0, __uint_as_float(sr[124]), __uint_as_float(sr[125]));
+      a1 = fmax3(a1, __uint_as_float(sr[126]), __uint_as_float(sr[127]));
+      const float mx = fmax3(a0, a1, fmaxf(a2, a3));
       const float m_new = fmaxf(m2, mx * sl2);
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
       const float alpha = ex2(m2 - mb);
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pr[64];
+      const uint64_t nmb2 = f2_pack(-mb, -mb);
+      uint64_t rs_a = f2_pack(0.f, 0.f), rs_b = rs_a;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), sl2, -mb));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -mb));
-        rs0 += p0;
-        rs1 += p1;
-        pr[i] = pack_bf16(p0, p1);
-      }
-      l = fmaf(alpha, l, rs0 + rs1);
-      tmem_st_x64(tmem + lane_addr + col_s, pr);
-      if (j > 0) {
-        // U must hold the previous tile's contribution before it is rescaled.
-        ok = wait_all(BAR(C::B_OD), (j - 1) & 1, abort_flag, budget);
-        if (!ok) break;
-        tc_fence_after();
-        if (!__all_sync(0xffffffffu, alpha == 1.f)) {
-          uint32_t ur[D];
-          tmem_ld_row<D>(tmem + lane_addr + kColO, ur);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pr[32];
 #pragma unroll
-          for (int i = 0; i < D; ++i) ur[i] = __float_as_uint(__uint_as_float(ur[i]) * alpha);
-          tmem_st_row<D>(tmem + lane_addr + kColO, ur);
+        for (int i = 0; i < 32; i += 2) {
+          const int e = 64 * h + 2 * i;
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2), x2, x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          rs_a = f2_add(rs_a, f2_pack(p0, p1));
+          rs_b = f2_add(rs_b, f2_pack(p2, p3));
+          pr[i] = pack_bf16(p0, p1);
+          pr[i + 1] = pack_bf16(p2, p3);
         }
+        tmem_st_x32(t_s + 32 * h, pr);  // P~ keys 64h..64h+63 -> columns 32h..32h+31
       }
+      float s0, s1, s2, s3;
+      f2_unpack(rs_a, s0, s1);
+      f2_unpack(rs_b, s2, s3);
+      l = fmaf(alpha, l, (s0 + s1) + (s2 + s3));
+      // PV_t(j-1) is complete (the commit that announced S_t(j) covers it): rescale U_t in place.
+      if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) rescale_row<D>(t_o, alpha);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(BAR(C::B_PF + b));
+      mbar_arrive(BAR(C::B_PF + t));
       m2 = m_new;
     }
-    if (ok) ok = wait_all(BAR(C::B_OD), (n_kv - 1) & 1, abort_flag, budget);
+    if (ok) ok = wait_all(BAR(C::B_SF + t), n & 1, abort_flag, budget);  // U_t final
     if (ok) {
       tc_fence_after();
-      uint32_t ur[D];
-      tmem_ld_row<D>(tmem + lane_addr + kColO, ur);
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      if (row < N) {
-        const size_t off = (static_cast<size_t>(bh) * N + row) * D;
-        if (o_fp32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + off);
-#pragma unroll
-          for (int i = 0; i < D / 4; ++i)
-            dst[i] = make_float4(__uint_as_float(ur[4 * i]) * inv, __uint_as_float(ur[4 * i + 1]) * inv,
-                                 __uint_as_float(ur[4 * i + 2]) * inv, __uint_as_float(ur[4 * i + 3]) * inv);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + off);
-#pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(ur[8 * i + 0]) * inv, __uint_as_float(ur[8 * i + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(ur[8 * i + 2]) * inv, __uint_as_float(ur[8 * i + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(ur[8 * i + 4]) * inv, __uint_as_float(ur[8 * i + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(ur[8 * i + 6]) * inv, __uint_as_float(ur[8 * i + 7]) * inv);
-            dst[i] = w;
-          }
-        }
-        lse[static_cast<size_t>(bh) * N + row] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
-      }
+      store_row<D>(o, lse, static_cast<size_t>(bh) * N + row, row < N, o_fp32 != 0, t_o, l, m2);
     }
     tmem_wait_st();
   }
 #undef BAR
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -323,8 +404,8 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
   auto kern = fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
-  const int n_tiles = (a.N + kBr - 1) / kBr;
-  dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_tiles));
+  const int n_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
+  dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
   kern<<<grid, kThreads, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget);
   return cudaGetLastError();
 }

@@ -90,23 +90,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
   }
 }
 
-// U_t row *= alpha, 32 columns at a time.
+// U_t row *= alpha, in one TMEM round trip.
 template <int D>
 __device__ __forceinline__ void rescale_row(uint32_t taddr, float alpha) {
   const uint64_t a2 = f2_pack(alpha, alpha);
+  uint32_t ur[D];
+  if constexpr (D == 128) tmem_ld_x128(taddr, ur); else tmem_ld_x64(taddr, ur);
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t ur[32];
-    tmem_ld_x32(taddr + 32 * c, ur);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float lo, hi;
-      f2_unpack(f2_mul(f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1])), a2), lo, hi);
-      ur[2 * i] = __float_as_uint(lo);
-      ur[2 * i + 1] = __float_as_uint(hi);
-    }
-    tmem_st_x32(taddr + 32 * c, ur);
+  for (int i = 0; i < D / 2; ++i) {
+    float lo, hi;
+    f2_unpack(f2_mul(f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1])), a2), lo, hi);
+    ur[2 * i] = __float_as_uint(lo);
+    ur[2 * i + 1] = __float_as_uint(hi);
   }
+  if constexpr (D == 128) tmem_st_x128(taddr, ur); else tmem_st_x64(taddr, ur);
 }
 
 // O row = U row / l to global memory, lse.  Every lane of the warp runs the

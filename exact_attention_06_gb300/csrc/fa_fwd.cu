@@ -14,13 +14,16 @@
 //
 // Warp roles (the producer/consumer split and the two-consumer "ping-pong" of
 // triton-tutorial §8.10.2-§8.10.3, re-done with TMA + tcgen05 + TMEM):
-//   warps 0-3  softmax of Q_0: thread r owns row r of the tile (TMEM lane r),
-//              so no cross-thread row reduction is needed (iceferryling
-//              "FlashAttention 1 和 FlashAttention 2 的区别", §7-8 split-Q); it
-//              also applies the alpha rescale of U_0 and writes O_0, lse.
-//   warps 4-7  the same for Q_1.
-//   warp 8     MMA issuer (one thread) and TMEM owner.
-//   warp 9     TMA producer: Q_0, Q_1 once, then K_j and V_j into two rings.
+//   warps 0-7  softmax of Q_0: two threads per query row, each with half of
+//              the row's 128 key columns (the .16x32bx2 TMEM access shape gives
+//              a warp 16 rows x both halves); the row max is joined with one
+//              shuffle, l is kept per half until the epilogue.  Whole rows stay
+//              inside one warp, so there is no cross-warp softmax merge
+//              (iceferryling "FlashAttention 1 和 FlashAttention 2 的区别", §7-8
+//              split-Q).  They also apply the alpha rescale of U_0 and write O_0, lse.
+//   warps 8-15 the same for Q_1.
+//   warp 16    MMA issuer (one thread) and TMEM owner.
+//   warp 17    TMA producer: Q_0, Q_1 once, then K_j and V_j into two rings.
 // The tensor core alternates between the tiles: [PV_0(j-1), S_0(j)] runs while
 // the Q_1 softmax works on S_1(j-1), and [PV_1(j-1), S_1(j)] while the Q_0
 // softmax works on S_0(j).  The commit after S_t(j) also covers PV_t(j-1), so
@@ -48,8 +51,9 @@ constexpr int kBr = 128;                 // query rows per tile (TMEM lanes, MMA
 constexpr int kBc = 128;                 // keys per tile
 constexpr int kRowsPerCta = 2 * kBr;
 constexpr uint32_t kBox = 128u * 128u;   // bytes of a 128-row x 64-column bf16 box
-constexpr int kThreads = 320;
-constexpr int kWarpMma = 8, kWarpTma = 9;
+constexpr int kSoftmaxWarps = 8;                      // per query tile
+constexpr int kThreads = (2 * kSoftmaxWarps + 2) * 32;  // 576
+constexpr int kWarpMma = 2 * kSoftmaxWarps, kWarpTma = kWarpMma + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -62,7 +66,12 @@ struct FwdCfg {
   static constexpr uint32_t QB = NH * kBox;         // bytes of one Q tile
   static constexpr uint32_t KVB = NH * kBox;        // bytes of one K (or V) tile
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
-                       B_SF = B_VE + VST, B_PF = B_SF + 2, B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;
+                       B_SF = B_VE + VST, B_PF = B_SF + 2, B_SC = B_PF + 2, B_OF = B_SC + 2, B_DRAIN = B_OF + 2,
+                       NBAR = B_DRAIN + 1;
+  // d = 64 leaves 128 TMEM columns free: P~_t gets its own columns there, so S_t(j+1) can be
+  // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S.
+  static constexpr bool SEP = (D == 64);
+  static constexpr uint32_t COL_P = SEP ? 384u : 0u;  // + 64 t (separate) or + 128 t (aliased)
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2 * QB;
   static constexpr uint32_t OFF_V = OFF_K + KST * KVB;
@@ -90,53 +99,51 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
   }
 }
 
-// U_t row *= alpha, in one TMEM round trip.
+// This thread's half of a U_t row (D/2 columns) *= alpha, in one TMEM round trip.
 template <int D>
-__device__ __forceinline__ void rescale_row(uint32_t taddr, float alpha) {
+__device__ __forceinline__ void rescale_half_row(uint32_t taddr, float alpha) {
   const uint64_t a2 = f2_pack(alpha, alpha);
-  uint32_t ur[D];
-  if constexpr (D == 128) tmem_ld_x128(taddr, ur); else tmem_ld_x64(taddr, ur);
+  uint32_t ur[D / 2];
+  if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
 #pragma unroll
-  for (int i = 0; i < D / 2; ++i) {
+  for (int i = 0; i < D / 4; ++i) {
     float lo, hi;
     f2_unpack(f2_mul(f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1])), a2), lo, hi);
     ur[2 * i] = __float_as_uint(lo);
     ur[2 * i + 1] = __float_as_uint(hi);
   }
-  if constexpr (D == 128) tmem_st_x128(taddr, ur); else tmem_st_x64(taddr, ur);
+  if constexpr (D == 128) tmem_st2_x64<64>(taddr, ur); else tmem_st2_x32<32>(taddr, ur);
 }
 
-// O row = U row / l to global memory, lse.  Every lane of the warp runs the
-// TMEM loads (tcgen05.ld is warp-collective); only rows < N are stored.
+// This thread's half of an O row = U / l to global memory (columns h*D/2 ..), and
+// lse from the h = 0 thread.  Every lane runs the TMEM load (it is warp-collective);
+// only rows < N are stored.
 template <int D>
-__device__ __forceinline__ void store_row(void* o, float* lse, size_t row_off, bool valid, bool o_fp32,
-                                          uint32_t taddr, float l, float m2) {
+__device__ __forceinline__ void store_half_row(void* o, float* lse, size_t row_off, int h, bool valid, bool o_fp32,
+                                               uint32_t taddr, float l, float m2) {
+  uint32_t ur[D / 2];
+  if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
+  if (!valid) return;
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  if (o_fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + row_off * D + h * (D / 2));
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t ur[32];
-    tmem_ld_x32(taddr + 32 * c, ur);
-    if (!valid) continue;
-    if (o_fp32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + row_off * D + 32 * c);
+    for (int i = 0; i < D / 8; ++i)
+      dst[i] = make_float4(__uint_as_float(ur[4 * i]) * inv, __uint_as_float(ur[4 * i + 1]) * inv,
+                           __uint_as_float(ur[4 * i + 2]) * inv, __uint_as_float(ur[4 * i + 3]) * inv);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + row_off * D + h * (D / 2));
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[i] = make_float4(__uint_as_float(ur[4 * i]) * inv, __uint_as_float(ur[4 * i + 1]) * inv,
-                             __uint_as_float(ur[4 * i + 2]) * inv, __uint_as_float(ur[4 * i + 3]) * inv);
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + row_off * D + 32 * c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 w;
-        w.x = pack_bf16(__uint_as_float(ur[8 * i + 0]) * inv, __uint_as_float(ur[8 * i + 1]) * inv);
-        w.y = pack_bf16(__uint_as_float(ur[8 * i + 2]) * inv, __uint_as_float(ur[8 * i + 3]) * inv);
-        w.z = pack_bf16(__uint_as_float(ur[8 * i + 4]) * inv, __uint_as_float(ur[8 * i + 5]) * inv);
-        w.w = pack_bf16(__uint_as_float(ur[8 * i + 6]) * inv, __uint_as_float(ur[8 * i + 7]) * inv);
-        dst[i] = w;
-      }
+    for (int i = 0; i < D / 16; ++i) {
+      uint4 w;
+      w.x = pack_bf16(__uint_as_float(ur[8 * i + 0]) * inv, __uint_as_float(ur[8 * i + 1]) * inv);
+      w.y = pack_bf16(__uint_as_float(ur[8 * i + 2]) * inv, __uint_as_float(ur[8 * i + 3]) * inv);
+      w.z = pack_bf16(__uint_as_float(ur[8 * i + 4]) * inv, __uint_as_float(ur[8 * i + 5]) * inv);
+      w.w = pack_bf16(__uint_as_float(ur[8 * i + 6]) * inv, __uint_as_float(ur[8 * i + 7]) * inv);
+      dst[i] = w;
     }
   }
-  if (valid) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
+  if (h == 0) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
 }
 
 template <int D, bool CAUSAL>
@@ -179,7 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR(C::B_SF + t), 1);
-      mbar_init(BAR(C::B_PF + t), kBr);
+      mbar_init(BAR(C::B_PF + t), kSoftmaxWarps * 32);
+      mbar_init(BAR(C::B_SC + t), kSoftmaxWarps * 32);
+      mbar_init(BAR(C::B_OF + t), 1);
     }
     mbar_init(BAR(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -235,25 +244,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);  // S = Q K^T, both K-major
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);    // U += P V, V is MN-major
+      // Descriptors computed once; each MMA below is one 32-bit add plus the tcgen05.mma.
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t qb = sQ + t * C::QB;
-        const uint32_t kb = sK + (j % C::KST) * C::KVB;
+        const uint64_t dq = sdesc_add(dq0, t * C::QB);
+        const uint64_t dk = sdesc_add(dk0, (j % C::KST) * C::KVB);
+        const uint32_t d_s = tmem + t * kBc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
-          mma_ss(tmem + t * kBc, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
+          if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
         }
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = sV + (j % C::VST) * C::KVB;
+        const uint64_t dv = sdesc_add(dv0, (j % C::VST) * C::KVB);
+        const uint32_t a_p = tmem + (C::SEP ? C::COL_P + 64u * t : static_cast<uint32_t>(t * kBc));
+        const uint32_t d_o = tmem + kColO + t * D;
+        // 16 keys per MMA: 16 rows x 128 B of each 64-column V box; boxes kBox apart along d.
+        if (j > 0) mma_ts_c<1>(d_o, a_p, dv, idesc_o);
+        else mma_ts_c<0>(d_o, a_p, dv, idesc_o);
 #pragma unroll
-        for (int kk = 0; kk < kBc / 16; ++kk) {
-          // 16 keys per MMA: 16 rows x 128 B of each 64-column V box; boxes kBox apart along d.
-          mma_ts(tmem + kColO + t * D, tmem + t * kBc + static_cast<uint32_t>(kk) * 8u,
-                 sdesc_sw128(vb + static_cast<uint32_t>(kk) * 2048u, kBox, 1024), idesc_o,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kBc / 16; ++kk)
+          mma_ts_c<1>(d_o, a_p + static_cast<uint32_t>(kk) * 8u, sdesc_add(dv, static_cast<uint32_t>(kk) * 2048u),
+                      idesc_o);
       };
       bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, budget, &g_fwd_status) &&
                 mbar_wait(BAR(C::B_KF), 0, abort_flag, budget, &g_fwd_status);
@@ -267,7 +283,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         tc_commit(BAR(C::B_KE));
       }
-      for (int j = 1; ok && j <= n_max; ++j) {
+      if constexpr (C::SEP) {
+        // S_t(j+1) as soon as the tile's softmax has read S_t(j); PV_t(j) once P~_t(j) is in TMEM.
+        for (int j = 0; ok && j < n_max; ++j) {
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nt = t ? n_t1 : n_t0;
+            if (!ok || j + 1 >= nt) continue;
+            if (!mbar_wait(BAR(C::B_SC + t), j & 1, abort_flag, budget, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            if (!k_ready) {
+              const int ks = (j + 1) % C::KST;
+              if (!mbar_wait(BAR(C::B_KF + ks), ((j + 1) / C::KST) & 1, abort_flag, budget, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              k_ready = true;
+            }
+            tc_fence_after();
+            issue_s(t, j + 1);
+            tc_commit(BAR(C::B_SF + t));
+          }
+          if (!ok) break;
+          if (k_ready) tc_commit(BAR(C::B_KE + (j + 1) % C::KST));
+          bool v_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nt = t ? n_t1 : n_t0;
+            if (!ok || j >= nt) continue;
+            if (!mbar_wait(BAR(C::B_PF + t), j & 1, abort_flag, budget, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            if (!v_ready) {
+              const int vs = j % C::VST;
+              if (!mbar_wait(BAR(C::B_VF + vs), (j / C::VST) & 1, abort_flag, budget, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              v_ready = true;
+            }
+            tc_fence_after();
+            issue_pv(t, j);
+            tc_commit(BAR(C::B_OF + t));  // PV_t(j) done: P~_t free again, U_t stable
+          }
+          if (!ok) break;
+          tc_commit(BAR(C::B_VE + j % C::VST));
+        }
+      }
+      for (int j = 1; !C::SEP && ok && j <= n_max; ++j) {
         bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -310,53 +377,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(BAR(C::B_DRAIN), 0, budget);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 0-7
-    const int t = warp >> 2;                      // query tile of this warpgroup
-    const int r = threadIdx.x - t * kBr;          // TMEM lane = row within the tile
+    // ------------------------------------------------------------ softmax warps 0-15
+    const int t = warp / kSoftmaxWarps;           // query tile of this warp
+    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+    const int sub = (warp % kSoftmaxWarps) >> 2;  // which 16 lanes of the quarter
+    const int h = lane >> 4;                      // which half of the row's columns
+    const int r = 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = row within the tile
     const int row = pair * kRowsPerCta + t * kBr + r;
     const int n = t ? n_t1 : n_t0;
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
     const uint32_t t_s = tmem + lane_addr + static_cast<uint32_t>(t * kBc);
     const uint32_t t_o = tmem + lane_addr + kColO + static_cast<uint32_t>(t * D);
+    const uint32_t t_p = tmem + lane_addr + C::COL_P + 64u * t;  // separate P~ columns (d = 64)
     const int lim = CAUSAL ? min(row, N - 1) : N - 1;  // last admissible key of this row
     const uint64_t c2 = f2_pack(sl2, sl2);
-    float m2 = -INFINITY, l = 0.f;
+    float m2 = -INFINITY, l = 0.f;  // l: this thread's half of the row
     bool ok = n > 0;
     for (int j = 0; ok && j < n; ++j) {
       ok = wait_all(BAR(C::B_SF + t), j & 1, abort_flag, budget);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld_x128(t_s, sr);
-      const int nvalid = lim - j * kBc + 1;  // admissible keys of this tile for this row
-      if (nvalid < kBc) {
+      uint32_t sr[64];
+      tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
+      if constexpr (C::SEP) {
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_SC + t));  // S_t(j) is in registers: the MMA may overwrite it
+      }
+      const int nvalid = lim - j * kBc - 64 * h + 1;  // admissible keys among them
+      if (nvalid < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
       }
       float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
       float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
 #pragma unroll
-      for (int i = 4; i < 124; i += 8) {
+      for (int i = 4; i < 60; i += 8) {
         a0 = fmax3(a0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
         a1 = fmax3(a1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
         a2 = fmax3(a2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
         a3 = fmax3(a3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
       }
-      a0 = fmax3(a0, __uint_as_float(sr[124]), __uint_as_float(sr[125]));
-      a1 = fmax3(a1, __uint_as_float(sr[126]), __uint_as_float(sr[127]));
-      const float mx = fmax3(a0, a1, fmaxf(a2, a3));
+      a0 = fmax3(a0, __uint_as_float(sr[60]), __uint_as_float(sr[61]));
+      a1 = fmax3(a1, __uint_as_float(sr[62]), __uint_as_float(sr[63]));
+      float mx = fmax3(a0, a1, fmaxf(a2, a3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // join the two halves of the row
       const float m_new = fmaxf(m2, mx * sl2);
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
       const float alpha = ex2(m2 - mb);
       const uint64_t nmb2 = f2_pack(-mb, -mb);
       uint64_t rs_a = f2_pack(0.f, 0.f), rs_b = rs_a;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pr[32];
+      if constexpr (C::SEP) {
+        // P~ packed in place into sr[0..31] (entry i holds keys 64h + 2i, 2i + 1).
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int e = 64 * h + 2 * i;
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2,
+                    x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          rs_a = f2_add(rs_a, f2_pack(p0, p1));
+          rs_b = f2_add(rs_b, f2_pack(p2, p3));
+          sr[i] = pack_bf16(p0, p1);
+          sr[i + 1] = pack_bf16(p2, p3);
+        }
+        // PV_t(j-1) must be done before P~_t(j) overwrites P~_t(j-1) and before U_t is rescaled.
+        if (j > 0) {
+          ok = wait_all(BAR(C::B_OF + t), (j - 1) & 1, abort_flag, budget);
+          if (!ok) break;
+          tc_fence_after();
+          if (!__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
+        }
+        uint32_t pr[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pr[i] = sr[i];
+        tmem_st2_x32<32>(t_p, pr);
+      }
+#pragma unroll
+      for (int q = 0; q < (C::SEP ? 0 : 2); ++q) {
+        uint32_t pr[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const int e = 32 * q + 2 * i;
           float x0, x1, x2, x3;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2), x0, x1);
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2), x2, x3);
@@ -366,23 +468,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[i] = pack_bf16(p0, p1);
           pr[i + 1] = pack_bf16(p2, p3);
         }
-        tmem_st_x32(t_s + 32 * h, pr);  // P~ keys 64h..64h+63 -> columns 32h..32h+31
+        // P~ keys 64h + 32q .. +31 -> packed columns 32h + 16q .. +15
+        tmem_st2_x16<32>(t_s + 16 * q, pr);
       }
       float s0, s1, s2, s3;
       f2_unpack(rs_a, s0, s1);
       f2_unpack(rs_b, s2, s3);
       l = fmaf(alpha, l, (s0 + s1) + (s2 + s3));
       // PV_t(j-1) is complete (the commit that announced S_t(j) covers it): rescale U_t in place.
-      if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) rescale_row<D>(t_o, alpha);
+      if (!C::SEP && j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(C::B_PF + t));
       m2 = m_new;
     }
-    if (ok) ok = wait_all(BAR(C::B_SF + t), n & 1, abort_flag, budget);  // U_t final
+    if (ok) {  // U_t final
+      if constexpr (C::SEP) ok = wait_all(BAR(C::B_OF + t), (n - 1) & 1, abort_flag, budget);
+      else ok = wait_all(BAR(C::B_SF + t), n & 1, abort_flag, budget);
+    }
     if (ok) {
       tc_fence_after();
-      store_row<D>(o, lse, static_cast<size_t>(bh) * N + row, row < N, o_fp32 != 0, t_o, l, m2);
+      const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2);
     }
     tmem_wait_st();
   }

@@ -51,9 +51,8 @@ constexpr int kBr = 128;                 // query rows per tile (TMEM lanes, MMA
 constexpr int kBc = 128;                 // keys per tile
 constexpr int kRowsPerCta = 2 * kBr;
 constexpr uint32_t kBox = 128u * 128u;   // bytes of a 128-row x 64-column bf16 box
-constexpr int kSoftmaxWarps = 8;                      // per query tile
-constexpr int kThreads = (2 * kSoftmaxWarps + 2) * 32;  // 576
-constexpr int kWarpMma = 2 * kSoftmaxWarps, kWarpTma = kWarpMma + 1;
+constexpr int kSoftmaxWarps = 8;          // per query tile
+constexpr int kWarpMma = 2 * kSoftmaxWarps;  // first MMA warp; also allocates TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -67,11 +66,17 @@ struct FwdCfg {
   static constexpr uint32_t KVB = NH * kBox;        // bytes of one K (or V) tile
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
                        B_SF = B_VE + VST, B_PF = B_SF + 2, B_SC = B_PF + 2, B_OF = B_SC + 2, B_DRAIN = B_OF + 2,
-                       NBAR = B_DRAIN + 1;
+                       NBAR = B_DRAIN + 2;
   // d = 64 leaves 128 TMEM columns free: P~_t gets its own columns there, so S_t(j+1) can be
   // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S.
   static constexpr bool SEP = (D == 64);
   static constexpr uint32_t COL_P = SEP ? 384u : 0u;  // + 64 t (separate) or + 128 t (aliased)
+  // At d = 64 the PV MMAs (N = 64) are too short for one issuing thread to keep the tensor core
+  // busy, so each tile gets its own MMA warp; at d = 128 one MMA warp alternating between the
+  // tiles measured faster.
+  static constexpr bool TWO_ISSUERS = (D == 64);
+  static constexpr int WARP_TMA = kWarpMma + (TWO_ISSUERS ? 2 : 1);
+  static constexpr int THREADS = (WARP_TMA + 1) * 32;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2 * QB;
   static constexpr uint32_t OFF_V = OFF_K + KST * KVB;
@@ -147,7 +152,7 @@ __device__ __forceinline__ void store_half_row(void* o, float* lse, size_t row_o
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, void* __restrict__ o, float* __restrict__ lse, int N,
                float sl2, int o_fp32, unsigned long long budget) {
@@ -176,13 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
+    // With an MMA warp per tile, each K (V) stage is released once by every tile that reads it.
+    const uint32_t users = C::TWO_ISSUERS ? (n_t0 > 0 ? 1u : 0u) + (n_t1 > 0 ? 1u : 0u) : 1u;
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(BAR(C::B_KF + s), 1);
-      mbar_init(BAR(C::B_KE + s), 1);
+      mbar_init(BAR(C::B_KE + s), users);
     }
     for (int s = 0; s < C::VST; ++s) {
       mbar_init(BAR(C::B_VF + s), 1);
-      mbar_init(BAR(C::B_VE + s), 1);
+      mbar_init(BAR(C::B_VE + s), users);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR(C::B_SF + t), 1);
@@ -191,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::B_OF + t), 1);
     }
     mbar_init(BAR(C::B_DRAIN), 1);
+    mbar_init(BAR(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == kWarpTma) {
+  if (warp == C::WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -239,9 +247,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = max(0, v_issued - C::VST); j < v_issued; ++j)
         drain_wait(BAR(C::B_VF + j % C::VST), (j / C::VST) & 1, budget);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (C::TWO_ISSUERS && (warp == kWarpMma || warp == kWarpMma + 1)) {
+    // ------------------------------------------------------------ MMA issuer of one tile
     if (lane == 0) {
+      const int t = warp - kWarpMma;
+      const int n = t ? n_t1 : n_t0;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
+      const uint64_t dq = sdesc_add(sdesc_sw128(sQ, 16, 1024), t * C::QB);
+      const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
+      const uint32_t d_s = tmem + t * kBc;
+      const uint32_t d_o = tmem + kColO + t * D;
+      const uint32_t a_p = tmem + (C::SEP ? C::COL_P + 64u * t : static_cast<uint32_t>(t * kBc));
+      auto issue_s = [&](int j) {
+        const uint64_t dk = sdesc_add(dk0, (j % C::KST) * C::KVB);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
+          if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+        }
+      };
+      auto issue_pv = [&](int j) {
+        const uint64_t dv = sdesc_add(dv0, (j % C::VST) * C::KVB);
+        if (j > 0) mma_ts_c<1>(d_o, a_p, dv, idesc_o);
+        else mma_ts_c<0>(d_o, a_p, dv, idesc_o);
+#pragma unroll
+        for (int kk = 1; kk < kBc / 16; ++kk)
+          mma_ts_c<1>(d_o, a_p + static_cast<uint32_t>(kk) * 8u, sdesc_add(dv, static_cast<uint32_t>(kk) * 2048u),
+                      idesc_o);
+      };
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        return mbar_wait(bar, parity, abort_flag, budget, &g_fwd_status);
+      };
+      bool ok = n > 0 && wait(BAR(C::B_Q), 0) && wait(BAR(C::B_KF), 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        tc_commit(BAR(C::B_SF + t));
+        tc_commit(BAR(C::B_KE));
+      }
+      if constexpr (C::SEP) {
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n) {
+            ok = wait(BAR(C::B_SC + t), j & 1) &&
+                 wait(BAR(C::B_KF + (j + 1) % C::KST), ((j + 1) / C::KST) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(j + 1);
+            tc_commit(BAR(C::B_SF + t));
+            tc_commit(BAR(C::B_KE + (j + 1) % C::KST));
+          }
+          ok = wait(BAR(C::B_PF + t), j & 1) && wait(BAR(C::B_VF + j % C::VST), (j / C::VST) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(j);
+          tc_commit(BAR(C::B_OF + t));
+          tc_commit(BAR(C::B_VE + j % C::VST));
+        }
+      } else {
+        for (int j = 1; ok && j <= n; ++j) {
+          ok = wait(BAR(C::B_PF + t), (j - 1) & 1) && wait(BAR(C::B_VF + (j - 1) % C::VST), ((j - 1) / C::VST) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(j - 1);
+          if (j < n) {
+            ok = wait(BAR(C::B_KF + j % C::KST), (j / C::KST) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(j);
+          }
+          tc_commit(BAR(C::B_SF + t));
+          tc_commit(BAR(C::B_VE + (j - 1) % C::VST));
+          if (j < n) tc_commit(BAR(C::B_KE + j % C::KST));
+        }
+      }
+      if (n > 0) {
+        tc_commit(BAR(C::B_DRAIN + t));
+        drain_wait(BAR(C::B_DRAIN + t), 0, budget);
+      }
+    }
+  } else if (!C::TWO_ISSUERS && warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer for both tiles
+    if constexpr (!C::TWO_ISSUERS) if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);  // S = Q K^T, both K-major
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);    // U += P V, V is MN-major
       // Descriptors computed once; each MMA below is one 32-bit add plus the tcgen05.mma.
@@ -283,58 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         tc_commit(BAR(C::B_KE));
       }
-      if constexpr (C::SEP) {
-        // S_t(j+1) as soon as the tile's softmax has read S_t(j); PV_t(j) once P~_t(j) is in TMEM.
-        for (int j = 0; ok && j < n_max; ++j) {
-          bool k_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int nt = t ? n_t1 : n_t0;
-            if (!ok || j + 1 >= nt) continue;
-            if (!mbar_wait(BAR(C::B_SC + t), j & 1, abort_flag, budget, &g_fwd_status)) {
-              ok = false;
-              break;
-            }
-            if (!k_ready) {
-              const int ks = (j + 1) % C::KST;
-              if (!mbar_wait(BAR(C::B_KF + ks), ((j + 1) / C::KST) & 1, abort_flag, budget, &g_fwd_status)) {
-                ok = false;
-                break;
-              }
-              k_ready = true;
-            }
-            tc_fence_after();
-            issue_s(t, j + 1);
-            tc_commit(BAR(C::B_SF + t));
-          }
-          if (!ok) break;
-          if (k_ready) tc_commit(BAR(C::B_KE + (j + 1) % C::KST));
-          bool v_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int nt = t ? n_t1 : n_t0;
-            if (!ok || j >= nt) continue;
-            if (!mbar_wait(BAR(C::B_PF + t), j & 1, abort_flag, budget, &g_fwd_status)) {
-              ok = false;
-              break;
-            }
-            if (!v_ready) {
-              const int vs = j % C::VST;
-              if (!mbar_wait(BAR(C::B_VF + vs), (j / C::VST) & 1, abort_flag, budget, &g_fwd_status)) {
-                ok = false;
-                break;
-              }
-              v_ready = true;
-            }
-            tc_fence_after();
-            issue_pv(t, j);
-            tc_commit(BAR(C::B_OF + t));  // PV_t(j) done: P~_t free again, U_t stable
-          }
-          if (!ok) break;
-          tc_commit(BAR(C::B_VE + j % C::VST));
-        }
-      }
-      for (int j = 1; !C::SEP && ok && j <= n_max; ++j) {
+      static_assert(!C::SEP, "the separate-P~ schedule runs with an MMA warp per tile");
+      for (int j = 1; ok && j <= n_max; ++j) {
         bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -510,7 +549,7 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
-  kern<<<grid, kThreads, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget);
   return cudaGetLastError();
 }
 

@@ -95,6 +95,8 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
 // Bounded wait that ignores the abort flag: used to drain in-flight copies
 // and MMAs before the CTA releases its shared memory and TMEM.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long budget) {
+  // A drain never gets less than the default budget, however short the caller's wait budget is.
+  if (budget < kDrainBudget) budget = kDrainBudget;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (static_cast<unsigned long long>(clock64() - t0) > budget) {

@@ -103,7 +103,7 @@ fa_status_t make_map(CUtensorMap* map, const void* base, int d, long long rows, 
   return FA_OK;
 }
 
-constexpr unsigned long long kDefaultBudget = 4000000000ull;  // SM cycles per wait (about 2 s)
+using fattn::kDefaultBudget;
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 

@@ -10,6 +10,10 @@ namespace fattn {
 
 // Bits of the per-device status word that kernels raise.
 constexpr unsigned int kStatusTimeout = 1u;
+// Default per-wait budget in SM cycles (about 2 s), and the least any drain of in-flight copies
+// and MMAs gets before a CTA releases its shared memory and TMEM.
+constexpr unsigned long long kDefaultBudget = 4000000000ull;
+constexpr unsigned long long kDrainBudget = kDefaultBudget;
 
 // Forward (prefill) launch description.  The tensor maps describe q, k, v as
 // 3-D tensors {d, N, B*H} (innermost first) with 64 x 128 boxes and 128-byte

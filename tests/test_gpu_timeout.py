@@ -1,0 +1,43 @@
+"""Failure detection on the GPU, without a fault: every wait in the kernels is
+bounded, and a wait that runs out ends the kernel with a status the host reads.
+
+fa_fwd_ex with a one-cycle wait budget makes the first waits of every CTA run
+out (the data they wait for cannot arrive within one cycle).  The kernel must
+report FA_ERR_TIMEOUT through fa_get_status, drain its in-flight copies and
+MMAs, free its TMEM, and leave the context usable: the next normal call on the
+same inputs must be correct.
+"""
+
+import math
+
+import pytest
+import torch
+
+import oracle
+from _util import assert_parity, ensure_built, run_fwd
+from exact_attention_06_gb300 import fattn, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_wait_budget_expiry_is_reported_and_the_context_survives(d, causal):
+    ensure_built()
+    B, H, N = 1, 4, 2000
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=21, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o = torch.zeros(B, H, N, d, dtype=torch.float32, device=DEV)
+    lse = torch.zeros(B, H, N, dtype=torch.float32, device=DEV)
+    fattn.fa_fwd_ex(q, k, v, o, lse, scale, causal, o_fp32=True, wait_budget_cycles=1)
+    with pytest.raises(fattn.FattnError) as err:
+        fattn.fa_get_status()
+    assert err.value.status == fattn.FA_ERR_TIMEOUT
+    assert fattn.fa_get_status() == fattn.FA_OK  # the status word was cleared by the read
+    # the same context still computes correct results
+    o2, lse2 = run_fwd(q, k, v, scale, causal, o_fp32=True)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), scale, causal,
+                                      rows=inputs.sample_rows(N, 256, seed=1).numpy())
+    rows = inputs.sample_rows(N, 256, seed=1)
+    assert_parity(o2[:, :, rows], lse2[:, :, rows], o_ref, lse_ref, "after a timeout")

@@ -148,6 +148,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's time (replicas: every rank runs the same step on its own GPU)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -286,11 +296,7 @@ def run_ours(args):
     ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush, sampler=sampler, dist_sync=dist_sync)
     sampler.stop()
     t_local = statistics.mean(ms)
-    t = t_local
-    if dist is not None:
-        tt = torch.tensor([t_local], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t_local, dist, dev)
     flops = w.flops()
     value = flops * world / (t * 1e-3) / 1e12
 

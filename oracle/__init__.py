@@ -7,7 +7,10 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
 from .attention import (  # noqa: F401
     admissible_keys,
     attention,
+    attention_backward,
+    attention_backward_head,
     attention_head,
+    backward_delta,
     chunk_partials,
     combine,
     compositions,

@@ -28,6 +28,12 @@ What it computes, and where the pages define it
   l = sum_w exp(m_w - m) l_w, O = sum_w exp(m_w - m) U_w / l (iceferryling
   "FlashAttention 1 和 FlashAttention 2 的区别", §6 cross-warp merge; the same
   rule reduces FlashDecoding partials, cnblogs jzssuanfa page, §三 场景 B).
+* ``attention_backward_head`` / ``attention_backward`` -- gradients of the
+  plain definition given dO: dV = P^T dO, dP = dO V^T, D_i = rowsum(dP_i * P_i)
+  (= rowsum(O_i * dO_i)), dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q
+  (triton-tutorial "8. FlashAttention 实战", §8.8.1 gradient formulas and
+  §8.8.3 D_i and dS; operatorworld "反向传播：用重算换显存").  P is formed
+  explicitly here; the blockwise recomputation from lse is the GPU's business.
 * ``chunk_partials`` / ``decode`` -- FlashDecoding split-K: one query row, the
   KV sequence cut into chunks, one partial (U, m, l) per chunk by the plain
   definition restricted to the chunk (cnblogs §三 场景 B, step 2).
@@ -42,8 +48,9 @@ design notes):
   §4; triton-tutorial §8.4.5).  The cnblogs page's block-local normalisation
   gives the same result.
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against values
-the pages print, closed forms, invariants, a library routine and brute force.
+Every function here is pinned by ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_backward_pins.py`` against values the pages print, closed
+forms, invariants, a library routine and brute force.
 """
 
 from __future__ import annotations
@@ -280,3 +287,50 @@ def decode(q, k, v, scale: float, pairs=None):
         o, ls = attention_head(_f64(q[b, h])[None, :], _f64(k[b, h]), _f64(v[b, h]), scale, False)
         out[idx], lse[idx] = o[0], ls[0]
     return out, lse
+
+
+def attention_backward_head(q, k, v, do, scale: float, causal: bool = False):
+    """Gradients of O = softmax(scale q k^T) v for one head, fp64.
+
+    q [N, d], k/v [Nk, d], do [N, dv] -> (dq [N, d], dk [Nk, d], dv [Nk, dv]).
+    Triton-tutorial §8.8.1: dV = P^T dO, dP = dO V^T; §8.8.3:
+    D_i = sum_j P_ij dP_ij, dS_ij = P_ij (dP_ij - D_i); dQ = scale dS K,
+    dK = scale dS^T Q.  Masked pairs have P = 0 and so dS = 0; a query row
+    with no admissible key gets zero gradient.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    n, nk = q.shape[0], k.shape[0]
+    s = float(scale) * (q @ k.T)
+    if causal:
+        s = np.where(np.arange(nk)[None, :] > np.arange(n)[:, None], NEG_INF, s)
+    p = np.zeros_like(s)
+    for i in range(n):
+        row = s[i]
+        if np.all(np.isneginf(row)):
+            continue
+        e = np.exp(row - row.max())
+        p[i] = e / e.sum()
+    dv = p.T @ do
+    dp = do @ v.T
+    dd = (dp * p).sum(axis=1)
+    ds = p * (dp - dd[:, None])
+    dq = float(scale) * (ds @ k)
+    dk = float(scale) * (ds.T @ q)
+    return dq, dk, dv
+
+
+def attention_backward(q, k, v, do, scale: float, causal: bool = False):
+    """attention_backward_head over [B, H, N, d] tensors; fp64 results."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            dq[b, h], dk[b, h], dv[b, h] = attention_backward_head(q[b, h], k[b, h], v[b, h], do[b, h], scale,
+                                                                   causal)
+    return dq, dk, dv
+
+
+def backward_delta(o, do):
+    """D_i = rowsum(O_i * dO_i) (triton-tutorial §8.8.3, the preprocess step)."""
+    return (_f64(o) * _f64(do)).sum(axis=-1)
+

@@ -192,6 +192,23 @@ def _decode_step_fn(w, dev, stream):
     return step, 2
 
 
+def _backward_step_fn(w, dev, stream):
+    """One backward (D, dK/dV, dQ kernels) over the workload, from a forward done once beforehand."""
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
+    do = inputs.normal_bf16(q.shape, seed=9, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    fattn.fa_fwd(q, k, v, o, lse, w.scale, w.causal, stream=stream)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fattn.fa_bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+
+    def step():
+        fattn.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, w.causal, workspace=ws, stream=stream)
+    return step, 3
+
+
 def _time_steps(step, steps, warmup, stream, flush=None, sampler=None, dist_sync=None):
     """Per-step CUDA-event times (ms) of exactly `steps` steps after `warmup` untimed ones."""
     import torch
@@ -328,6 +345,21 @@ def run_ours(args):
                 extra[name]["roofline"]["note"] = "duration covers the split kernel and the combine kernel"
             del st_fn
             torch.cuda.empty_cache()
+        # backward on the causal workload (NEXT row of the plan): 2.5x the forward's flops by the usual
+        # count (five N^2 d products); the dQ pass recomputes two of them, which is not counted
+        wb = inputs.WORKLOADS["causal"]
+        bst, nl = _backward_step_fn(wb, dev, stream)
+        bms = _time_steps(bst, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
+        bt = statistics.mean(bms)
+        bflops = 2.5 * wb.flops()
+        extra["backward_causal"] = {
+            "value": round(bflops / (bt * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s", "ms_per_step": round(bt, 4),
+            "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
+            "config": {"B": wb.B, "H": wb.H, "N": wb.N, "d": wb.d, "causal": True, "spike_every_64th_key_x8": True},
+            "roofline": _roofline("tensor", bflops, bt, peaks, None),
+            "note": "fa_bwd: rowsum(O*dO), dK/dV pass, dQ pass; flops = 2.5 x forward (algorithmic)"}
+        del bst
+        torch.cuda.empty_cache()
 
     e2e = _e2e_prefill(w, dev, stream, max(3, min(args.steps, 50)), max(3, args.warmup))
     if world > 1:
@@ -370,7 +402,7 @@ def run_ours(args):
 
 def run_only(args, w, dev, stream, peaks, flush):
     """One workload alone (profiler captures and sweeps): its step timed like the headline."""
-    fn = _decode_step_fn if w.kind == "decode" else _prefill_step_fn
+    fn = _decode_step_fn if w.kind == "decode" else (_backward_step_fn if args.backward else _prefill_step_fn)
     step, launches = fn(w, dev, stream)
     small = w.kind == "prefill" and 3 * w.B * w.H * w.N * w.d * 2 < L2_FLUSH_BYTES
     ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush if small else None)
@@ -379,9 +411,10 @@ def run_only(args, w, dev, stream, peaks, flush):
         work, kind, kern, unit = w.kv_bytes(), "hbm", "decode_split_kernel", "GB/s"
         value = work / (t * 1e-3) / 1e9
     else:
-        work, kind, kern, unit = w.flops(), "tensor", "fwd_kernel", "TFLOP/s"
+        work = w.flops() * (2.5 if args.backward else 1.0)
+        kind, kern, unit = "tensor", ("bwd" if args.backward else "fwd_kernel"), "TFLOP/s"
         value = work / (t * 1e-3) / 1e12
-    print(json.dumps({"workload": w.name, "value": round(value, 3), "unit": unit, "steps": args.steps,
+    print(json.dumps({"workload": w.name + (" backward" if args.backward else ""), "value": round(value, 3), "unit": unit, "steps": args.steps,
                       "warmup": args.warmup, "ms_per_step": round(t, 5), "ms_min": round(min(ms), 5),
                       "gpu_launches": launches * args.steps,
                       "roofline": _roofline(kind, work, t, peaks, _traffic(kern, w.name))}), flush=True)
@@ -486,6 +519,7 @@ def main():
     ap.add_argument("--extra-steps", type=int, default=20)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--only", default=None, help="time one named workload alone (e.g. causal, decode_small)")
+    ap.add_argument("--backward", action="store_true", help="with --only: time fa_bwd instead of the forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

@@ -1,0 +1,567 @@
+// Attention backward for sm_103a: gradients dQ, dK, dV from Q, K, V, O, dO and
+// the forward's lse, recomputing P blockwise instead of storing it
+// (triton-tutorial "8. FlashAttention 实战", §8.8.2-§8.8.4; operatorworld
+// "反向传播：用重算换显存"; xuesongtap.github.io "flash-attention", §3).
+//
+//   D_i    = rowsum(O_i * dO_i)                                   bwd_delta_kernel
+//   P_ij   = exp(S_ij * scale - lse_i)      S = Q K^T (recomputed)
+//   dP_ij  = dO_i V_j^T
+//   dS_ij  = P_ij (dP_ij - D_i)
+//   dV_j  += P_ij^T dO_i,   dK_j += scale dS_ij^T Q_i             bwd_dkdv_kernel (one CTA per key tile)
+//   dQ_i  += scale dS_ij K_j                                      bwd_dq_kernel   (one CTA per query tile)
+// Two passes instead of atomics on dQ: the tutorial's two-phase kernel
+// (§8.8.4) splits the same way; every output tile has one owner.
+//
+// Both main kernels keep their own tile resident in shared memory, stream the
+// other side through a TMA ring, compute the two products of a step with
+// tcgen05.mma into TMEM, let 8 elementwise warps (two threads per row, the
+// .16x32bx2 TMEM shape) turn them into bf16 P^T and dS^T (or dS) in TMEM, and
+// accumulate the gradient MMAs (A operand from TMEM) into TMEM.  The gradient
+// MMAs of step i and the products of step i+1 are issued back to back; the
+// tensor core runs them in order, so the products may overwrite the TMEM
+// columns the gradient MMAs read.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmem_io.cuh"
+
+namespace fattn {
+
+__device__ unsigned int g_bwd_status = 0;
+
+namespace {
+
+constexpr int kTile = 128;                // rows per tile on either side
+constexpr uint32_t kBox = 128u * 128u;    // bytes of a 128-row x 64-column bf16 box
+constexpr int kEwWarps = 8;               // elementwise warps: two threads per row
+constexpr int kWarpMma = kEwWarps, kWarpTma = kEwWarps + 1;
+constexpr int kThreads = (kEwWarps + 2) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA = 0, kColB = 128, kColG1 = 256;  // products at 0 / 128, gradients from 256
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned long long budget) {
+  return mbar_wait(bar, parity, abort_flag, budget, &g_bwd_status);
+}
+__device__ __forceinline__ bool bwait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long budget) {
+  return __all_sync(0xffffffffu, bwait(bar, parity, abort_flag, budget));
+}
+__device__ __forceinline__ void bdrain(uint32_t bar, uint32_t parity, unsigned long long budget) {
+  if (budget < kDrainBudget) budget = kDrainBudget;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (static_cast<unsigned long long>(clock64() - t0) > budget) {
+      atomicOr(&g_bwd_status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+// --------------------------------------------------------------------- D = rowsum(O * dO)
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, long long rows) {
+  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = gt / TPR;
+  const int part = static_cast<int>(gt % TPR);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[part];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[part];
+    acc = fmaf(bf16lo(a.x), bf16lo(b.x), acc);
+    acc = fmaf(bf16hi(a.x), bf16hi(b.x), acc);
+    acc = fmaf(bf16lo(a.y), bf16lo(b.y), acc);
+    acc = fmaf(bf16hi(a.y), bf16hi(b.y), acc);
+    acc = fmaf(bf16lo(a.z), bf16lo(b.z), acc);
+    acc = fmaf(bf16hi(a.z), bf16hi(b.z), acc);
+    acc = fmaf(bf16lo(a.w), bf16lo(b.w), acc);
+    acc = fmaf(bf16hi(a.w), bf16hi(b.w), acc);
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) delta[row] = acc;
+}
+
+// --------------------------------------------------------------------- shared pieces
+template <int D>
+struct BwdCfg {
+  static constexpr int NH = D / 64;
+  static constexpr uint32_t TB = NH * kBox;   // bytes of one 128 x d bf16 tile
+  static constexpr int ST = (D == 128) ? 2 : 4;
+  static constexpr uint32_t VEC = 2 * kTile * 4;  // lse2[128] + D[128] fp32 per stage (dkdv only)
+  static constexpr uint32_t COL_G2 = kColG1 + D;  // second gradient accumulator (dK)
+};
+
+// Gradient tile (TMEM, fp32, D columns) * scale -> global rows < N (bf16 or fp32), this thread's half row.
+template <int D>
+__device__ __forceinline__ void store_grad_half_row(void* out, size_t row_off, int h, bool valid, bool fp32,
+                                                    uint32_t taddr, float scale) {
+  uint32_t ur[D / 2];
+  if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
+  if (!valid) return;
+  if (fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off * D + h * (D / 2));
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      dst[i] = make_float4(__uint_as_float(ur[4 * i]) * scale, __uint_as_float(ur[4 * i + 1]) * scale,
+                           __uint_as_float(ur[4 * i + 2]) * scale, __uint_as_float(ur[4 * i + 3]) * scale);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row_off * D + h * (D / 2));
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      uint4 w;
+      w.x = pack_bf16(__uint_as_float(ur[8 * i + 0]) * scale, __uint_as_float(ur[8 * i + 1]) * scale);
+      w.y = pack_bf16(__uint_as_float(ur[8 * i + 2]) * scale, __uint_as_float(ur[8 * i + 3]) * scale);
+      w.z = pack_bf16(__uint_as_float(ur[8 * i + 4]) * scale, __uint_as_float(ur[8 * i + 5]) * scale);
+      w.w = pack_bf16(__uint_as_float(ur[8 * i + 6]) * scale, __uint_as_float(ur[8 * i + 7]) * scale);
+      dst[i] = w;
+    }
+  }
+}
+
+// S = A B^T into TMEM: A and B are resident/streamed 128 x d K-major tiles.
+template <int D>
+__device__ __forceinline__ void issue_product(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
+    if (kk == 0) mma_ss_c<0>(d_tmem, sdesc_add(da, off), sdesc_add(db, off), idesc);
+    else mma_ss_c<1>(d_tmem, sdesc_add(da, off), sdesc_add(db, off), idesc);
+  }
+}
+// Packed bf16 operands in TMEM keep each half of the 128-wide K dimension in its own half of
+// the 128 columns it was computed in: elements 0..63 at packed columns 0..31, elements 64..127 at
+// 64..95.  The elementwise threads that produce a half then only overwrite columns they have
+// already read.  Column of the k-th 16-element K block:
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? 8u * kk : 64u + 8u * (kk - 4); }
+
+// G (+)= X Y with X (128 x 128) packed bf16 in TMEM (layout above) and Y a 128 x d MN-major tile.
+template <int D>
+__device__ __forceinline__ void issue_grad(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idesc,
+                                           bool accumulate) {
+  if (accumulate) mma_ts_c<1>(d_tmem, a_tmem, db, idesc);
+  else mma_ts_c<0>(d_tmem, a_tmem, db, idesc);
+#pragma unroll
+  for (int kk = 1; kk < kTile / 16; ++kk)
+    mma_ts_c<1>(d_tmem, a_tmem + packed_col(kk), sdesc_add(db, static_cast<uint32_t>(kk) * 2048u), idesc);
+}
+
+// --------------------------------------------------------------------- dK, dV: one CTA per key tile
+// TMEM: S^T at 0 (P^T packed into it), dP^T at 128 (dS^T packed into it), dV at 256, dK at 256 + d.
+template <int D>
+struct DkdvCfg : BwdCfg<D> {
+  using B = BwdCfg<D>;
+  static constexpr uint32_t OFF_K = 0, OFF_V = B::TB;
+  static constexpr uint32_t OFF_RING = 2 * B::TB;                   // stage: Q_i, dO_i
+  static constexpr uint32_t STAGE = 2 * B::TB;
+  static constexpr uint32_t OFF_VEC = OFF_RING + B::ST * STAGE;     // stage: lse2[128], D[128]
+  static constexpr uint32_t OFF_BAR = OFF_VEC + B::ST * B::VEC;
+  static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
+                       B_DRAIN = B_PF + 1, NBAR = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
+  static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
+};
+static_assert(DkdvCfg<128>::SMEM <= 232448, "dK/dV kernel shared memory");
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dk,
+                    void* __restrict__ dv, int N, float sl2, float scale, int grad_fp32,
+                    unsigned long long budget) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sRing = base + C::OFF_RING, sBar = base + C::OFF_BAR;
+  float* vec = reinterpret_cast<float*>(gbase + C::OFF_VEC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+#define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int kt = blockIdx.y;  // key tile; small kt has the most causal work and is scheduled first
+  const int n_tiles = (N + kTile - 1) / kTile;
+  const int i0 = CAUSAL ? kt : 0;  // first query tile that sees this key tile
+  const int n_i = n_tiles - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_KV), 1);
+    for (int s = 0; s < C::ST; ++s) {
+      mbar_init(BAR(C::B_FULL + s), 1 + 32);  // TMA bytes + the producer warp's lse/D stores
+      mbar_init(BAR(C::B_EMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SF), 1);
+    mbar_init(BAR(C::B_PF), kEwWarps * 32);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ producer (whole warp)
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      mbar_arrive_expect_tx(BAR(C::B_KV), 2 * C::TB);
+      for (int h = 0; h < C::NH; ++h) {
+        tma_load_3d(sK + h * kBox, &tk, BAR(C::B_KV), h * 64, kt * kTile, bh);
+        tma_load_3d(sV + h * kBox, &tv, BAR(C::B_KV), h * 64, kt * kTile, bh);
+      }
+    }
+    int issued = 0;
+    for (int i = 0; i < n_i; ++i) {
+      const int s = i % C::ST;
+      if (i >= C::ST && !bwait_all(BAR(C::B_EMPTY + s), ((i / C::ST) - 1) & 1, abort_flag, budget)) break;
+      const int qt = i0 + i;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(BAR(C::B_FULL + s), 2 * C::TB);
+        const uint32_t st = sRing + s * C::STAGE;
+        for (int h = 0; h < C::NH; ++h) {
+          tma_load_3d(st + h * kBox, &tq, BAR(C::B_FULL + s), h * 64, qt * kTile, bh);
+          tma_load_3d(st + C::TB + h * kBox, &tdo, BAR(C::B_FULL + s), h * 64, qt * kTile, bh);
+        }
+      }
+      // lse (as log2 units) and D of the tile's 128 query rows; rows past N get lse = +inf, so P = 0.
+      float* vs = vec + s * (2 * kTile);
+#pragma unroll
+      for (int c = 0; c < kTile / 32; ++c) {
+        const int r = qt * kTile + 32 * c + lane;
+        const bool in = r < N;
+        vs[32 * c + lane] = in ? lse[static_cast<size_t>(bh) * N + r] * kLog2e : INFINITY;
+        vs[kTile + 32 * c + lane] = in ? delta[static_cast<size_t>(bh) * N + r] : 0.f;
+      }
+      mbar_arrive(BAR(C::B_FULL + s));
+      issued = i + 1;
+    }
+    if (lane == 0) {
+      bdrain(BAR(C::B_KV), 0, budget);
+      for (int i = max(0, issued - C::ST); i < issued; ++i) bdrain(BAR(C::B_FULL + i % C::ST), (i / C::ST) & 1, budget);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_p = idesc_bf16_f32(kTile, kTile, 0);  // K Q^T, V dO^T: both K-major
+      constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);      // P^T dO, dS^T Q: MN-major B
+      const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dR = sdesc_sw128(sRing, 16, 1024), dRmn = sdesc_sw128(sRing, kBox, 1024);
+      auto products = [&](int i) {
+        const uint32_t st = (i % C::ST) * C::STAGE;
+        issue_product<D>(tmem + kColA, dK, sdesc_add(dR, st), idesc_p);           // S^T = K Q^T
+        issue_product<D>(tmem + kColB, dV, sdesc_add(dR, st + C::TB), idesc_p);   // dP^T = V dO^T
+      };
+      bool ok = bwait(BAR(C::B_KV), 0, abort_flag, budget) && bwait(BAR(C::B_FULL), 0, abort_flag, budget);
+      if (ok) {
+        tc_fence_after();
+        products(0);
+        tc_commit(BAR(C::B_SF));
+      }
+      for (int i = 0; ok && i < n_i; ++i) {
+        if (!bwait(BAR(C::B_PF), i & 1, abort_flag, budget)) break;
+        tc_fence_after();
+        const uint32_t st = (i % C::ST) * C::STAGE;
+        issue_grad<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0);  // dV += P^T dO
+        issue_grad<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0);      // dK += dS^T Q
+        tc_commit(BAR(C::B_EMPTY + i % C::ST));
+        if (i + 1 < n_i) {
+          if (!bwait(BAR(C::B_FULL + (i + 1) % C::ST), ((i + 1) / C::ST) & 1, abort_flag, budget)) break;
+          tc_fence_after();
+          products(i + 1);
+        }
+        tc_commit(BAR(C::B_SF));  // next products ready (or the gradients final)
+      }
+      tc_commit(BAR(C::B_DRAIN));
+      bdrain(BAR(C::B_DRAIN), 0, budget);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warps: thread = key row
+    const int quarter = warp & 3, sub = warp >> 2, h = lane >> 4;
+    const int r = 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = key row within the tile
+    const int key = kt * kTile + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
+    const uint32_t tA = tmem + lane_addr + kColA, tB = tmem + lane_addr + kColB;
+    bool ok = true;
+    for (int i = 0; ok && i < n_i; ++i) {
+      const int s = i % C::ST;
+      ok = bwait_all(BAR(C::B_SF), i & 1, abort_flag, budget) &&
+           bwait_all(BAR(C::B_FULL + s), (i / C::ST) & 1, abort_flag, budget);
+      if (!ok) break;
+      tc_fence_after();
+      const int qt = i0 + i;
+      const float* lse2 = vec + s * (2 * kTile);
+      const float* dd = lse2 + kTile;
+      // this thread's 64 query columns, two chunks of 32
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld2_x32<64>(tA + 32 * c, sv);
+        tmem_ld2_x32<64>(tB + 32 * c, pv);
+        uint32_t pp[16], dp[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = 64 * h + 32 * c + e;        // query row within the tile
+          const int qrow = qt * kTile + col;
+          float p0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2[col]));
+          float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2[col + 1]));
+          if (CAUSAL) {
+            if (qrow < key) p0 = 0.f;
+            if (qrow + 1 < key) p1 = 0.f;
+          }
+          const float s0 = p0 * (__uint_as_float(pv[e]) - dd[col]);
+          const float s1 = p1 * (__uint_as_float(pv[e + 1]) - dd[col + 1]);
+          pp[e / 2] = pack_bf16(p0, p1);
+          dp[e / 2] = pack_bf16(s0, s1);
+        }
+        tmem_st2_x16<64>(tA + 16 * c, pp);  // P^T packed: columns 64h + 16c ..
+        tmem_st2_x16<64>(tB + 16 * c, dp);  // dS^T packed
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_PF));
+    }
+    if (ok) ok = bwait_all(BAR(C::B_SF), n_i & 1, abort_flag, budget);  // gradients final
+    if (ok) {
+      tc_fence_after();
+      const size_t row_off = static_cast<size_t>(bh) * N + key;
+      store_grad_half_row<D>(dv, row_off, h, key < N, grad_fp32 != 0, tmem + lane_addr + kColG1, 1.f);
+      store_grad_half_row<D>(dk, row_off, h, key < N, grad_fp32 != 0, tmem + lane_addr + C::COL_G2, scale);
+    }
+    tmem_wait_st();
+  }
+#undef BAR
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------- dQ: one CTA per query tile
+// TMEM: S at 0, dP at 128 (dS packed into it), dQ at 256.
+template <int D>
+struct DqCfg : BwdCfg<D> {
+  using B = BwdCfg<D>;
+  static constexpr uint32_t OFF_Q = 0, OFF_DO = B::TB;
+  static constexpr uint32_t OFF_RING = 2 * B::TB;  // stage: K_j, V_j
+  static constexpr uint32_t STAGE = 2 * B::TB;
+  static constexpr uint32_t OFF_BAR = OFF_RING + B::ST * STAGE;
+  static constexpr int B_QD = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
+                       B_DRAIN = B_PF + 1, NBAR = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
+  static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
+};
+static_assert(DqCfg<128>::SMEM <= 232448, "dQ kernel shared memory");
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dq, int N,
+                  float sl2, float scale, int grad_fp32, unsigned long long budget) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_Q, sDO = base + C::OFF_DO, sRing = base + C::OFF_RING, sBar = base + C::OFF_BAR;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+#define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int n_tiles = (N + kTile - 1) / kTile;
+  const int qt = n_tiles - 1 - static_cast<int>(blockIdx.y);  // most causal work first
+  const int n_j = CAUSAL ? qt + 1 : n_tiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_QD), 1);
+    for (int s = 0; s < C::ST; ++s) {
+      mbar_init(BAR(C::B_FULL + s), 1);
+      mbar_init(BAR(C::B_EMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SF), 1);
+    mbar_init(BAR(C::B_PF), kEwWarps * 32);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == kWarpTma) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      mbar_arrive_expect_tx(BAR(C::B_QD), 2 * C::TB);
+      for (int h = 0; h < C::NH; ++h) {
+        tma_load_3d(sQ + h * kBox, &tq, BAR(C::B_QD), h * 64, qt * kTile, bh);
+        tma_load_3d(sDO + h * kBox, &tdo, BAR(C::B_QD), h * 64, qt * kTile, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_j; ++j) {
+        const int s = j % C::ST;
+        if (j >= C::ST && !bwait(BAR(C::B_EMPTY + s), ((j / C::ST) - 1) & 1, abort_flag, budget)) break;
+        mbar_arrive_expect_tx(BAR(C::B_FULL + s), 2 * C::TB);
+        const uint32_t st = sRing + s * C::STAGE;
+        for (int h = 0; h < C::NH; ++h) {
+          tma_load_3d(st + h * kBox, &tk, BAR(C::B_FULL + s), h * 64, j * kTile, bh);
+          tma_load_3d(st + C::TB + h * kBox, &tv, BAR(C::B_FULL + s), h * 64, j * kTile, bh);
+        }
+        issued = j + 1;
+      }
+      bdrain(BAR(C::B_QD), 0, budget);
+      for (int j = max(0, issued - C::ST); j < issued; ++j) bdrain(BAR(C::B_FULL + j % C::ST), (j / C::ST) & 1, budget);
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_p = idesc_bf16_f32(kTile, kTile, 0);  // Q K^T, dO V^T: both K-major
+      constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);      // dS K: K MN-major
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dDO = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t dR = sdesc_sw128(sRing, 16, 1024), dRmn = sdesc_sw128(sRing, kBox, 1024);
+      auto products = [&](int j) {
+        const uint32_t st = (j % C::ST) * C::STAGE;
+        issue_product<D>(tmem + kColA, dQ, sdesc_add(dR, st), idesc_p);           // S = Q K^T
+        issue_product<D>(tmem + kColB, dDO, sdesc_add(dR, st + C::TB), idesc_p);  // dP = dO V^T
+      };
+      bool ok = bwait(BAR(C::B_QD), 0, abort_flag, budget) && bwait(BAR(C::B_FULL), 0, abort_flag, budget);
+      if (ok) {
+        tc_fence_after();
+        products(0);
+        tc_commit(BAR(C::B_SF));
+      }
+      for (int j = 0; ok && j < n_j; ++j) {
+        if (!bwait(BAR(C::B_PF), j & 1, abort_flag, budget)) break;
+        tc_fence_after();
+        issue_grad<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, j > 0);  // dQ += dS K
+        tc_commit(BAR(C::B_EMPTY + j % C::ST));
+        if (j + 1 < n_j) {
+          if (!bwait(BAR(C::B_FULL + (j + 1) % C::ST), ((j + 1) / C::ST) & 1, abort_flag, budget)) break;
+          tc_fence_after();
+          products(j + 1);
+        }
+        tc_commit(BAR(C::B_SF));
+      }
+      tc_commit(BAR(C::B_DRAIN));
+      bdrain(BAR(C::B_DRAIN), 0, budget);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warps: thread = query row
+    const int quarter = warp & 3, sub = warp >> 2, h = lane >> 4;
+    const int r = 32 * quarter + 16 * sub + (lane & 15);
+    const int row = qt * kTile + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
+    const uint32_t tA = tmem + lane_addr + kColA, tB = tmem + lane_addr + kColB;
+    const bool in = row < N;
+    const float lse2 = in ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : INFINITY;
+    const float dd = in ? delta[static_cast<size_t>(bh) * N + row] : 0.f;
+    const int lim = CAUSAL ? min(row, N - 1) : N - 1;  // last key this row attends
+    bool ok = true;
+    for (int j = 0; ok && j < n_j; ++j) {
+      ok = bwait_all(BAR(C::B_SF), j & 1, abort_flag, budget);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld2_x32<64>(tA + 32 * c, sv);
+        tmem_ld2_x32<64>(tB + 32 * c, pv);
+        uint32_t dp[16];
+        const int key0 = j * kTile + 64 * h + 32 * c;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2));
+          if (key0 + e > lim) p0 = 0.f;
+          if (key0 + e + 1 > lim) p1 = 0.f;
+          dp[e / 2] = pack_bf16(p0 * (__uint_as_float(pv[e]) - dd), p1 * (__uint_as_float(pv[e + 1]) - dd));
+        }
+        tmem_st2_x16<64>(tB + 16 * c, dp);  // dS packed into dP's columns 64h + 16c ..
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_PF));
+    }
+    if (ok) ok = bwait_all(BAR(C::B_SF), n_j & 1, abort_flag, budget);
+    if (ok) {
+      tc_fence_after();
+      store_grad_half_row<D>(dq, static_cast<size_t>(bh) * N + row, h, in, grad_fp32 != 0, tmem + lane_addr + kColG1,
+                             scale);
+    }
+    tmem_wait_st();
+  }
+#undef BAR
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.BH) * a.N;
+  const long long threads = rows * (D / 8);
+  bwd_delta_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.delta, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_tiles));
+  auto k1 = bwd_dkdv_kernel<D, CAUSAL>;
+  if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM)) != cudaSuccess)
+    return e;
+  k1<<<grid, kThreads, DkdvCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dk, a.dv, a.N,
+                                                   a.scale_log2, a.scale, a.grad_fp32, a.budget);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto k2 = bwd_dq_kernel<D, CAUSAL>;
+  if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM)) != cudaSuccess)
+    return e;
+  k2<<<grid, kThreads, DqCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dq, a.N, a.scale_log2,
+                                                 a.scale, a.grad_fp32, a.budget);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
+  return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+}
+
+unsigned int bwd_read_and_clear_status() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bwd_status, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace fattn

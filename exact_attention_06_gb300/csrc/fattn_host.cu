@@ -324,11 +324,66 @@ fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_
   return FA_OK;
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return round256(static_cast<size_t>(B) * H * N * sizeof(float));
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int grad_fp32,
+                   void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H and N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (grad_fp32 != 0 && grad_fp32 != 1) return fail(FA_ERR_INVALID_ARG, "grad_fp32 must be 0 or 1");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, dq, dk and dv must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
+  if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 tile grid limit", N);
+  const size_t need = fa_bwd_workspace_bytes(B, H, N);
+  if (!workspace || ws_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+  if (!aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  fa_status_t st = check_device(nullptr);
+  if (st != FA_OK) return st;
+  fattn::BwdLaunch a{};
+  if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tk, k, d, N, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v, d, N, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tdo, dout, d, N, bh, 128)) != FA_OK) return st;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = static_cast<float*>(workspace);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.N = N;
+  a.BH = static_cast<int>(bh);
+  a.d = d;
+  a.causal = causal;
+  a.grad_fp32 = grad_fp32;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.budget = kDefaultBudget;
+  cudaGetLastError();
+  cudaError_t e = fattn::launch_bwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
+  return FA_OK;
+}
+
 fa_status_t fa_get_status(void* stream) {
   g_last_error[0] = '\0';
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_get_status synchronize");
-  const unsigned int bits = fattn::fwd_read_and_clear_status() | fattn::decode_read_and_clear_status();
+  const unsigned int bits = fattn::fwd_read_and_clear_status() | fattn::decode_read_and_clear_status() |
+                            fattn::bwd_read_and_clear_status();
   if (bits & fattn::kStatusTimeout) return fail(FA_ERR_TIMEOUT, "a kernel wait exceeded its budget");
   return FA_OK;
 }

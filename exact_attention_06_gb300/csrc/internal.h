@@ -58,6 +58,29 @@ cudaError_t launch_combine(const float* u_part, const float* m_part, const float
                            int R, int S, int d, cudaStream_t stream);
 unsigned int decode_read_and_clear_status();
 
+// Backward launch description: q, k, v, dO as 3-D tensors {d, N, B*H} with
+// 64 x 128 boxes and 128-byte swizzle; delta is the caller's [B*H, N] fp32 scratch.
+struct BwdLaunch {
+  CUtensorMap tq, tk, tv, tdo;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* delta;
+  void* dq;
+  void* dk;
+  void* dv;
+  int N;
+  int BH;
+  int d;
+  int causal;
+  int grad_fp32;
+  float scale;
+  float scale_log2;
+  unsigned long long budget;
+};
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
+unsigned int bwd_read_and_clear_status();
+
 // Fixed device scratch used by fa_decode_splitkv_noalloc in place of a
 // caller-provided workspace.  Size limit of that entry point.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;

@@ -25,8 +25,9 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_decode_workspace_bytes", "fa_decode_splitkv", "fa_decode_splitkv_noalloc",
-            "fa_combine", "fa_get_status", "fa_status_string", "fa_last_error")
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
+            "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_combine", "fa_get_status", "fa_status_string",
+            "fa_last_error")
 FA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -53,6 +54,9 @@ def lib() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
+        L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+        L.fa_bwd_workspace_bytes.restype = sz
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
         L.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.fa_decode_workspace_bytes.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
@@ -63,8 +67,8 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_combine",
-                     "fa_get_status"):
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_decode_splitkv", "fa_decode_splitkv_noalloc",
+                     "fa_combine", "fa_get_status"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -118,6 +122,22 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None):
     st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
                       _stream(stream))
     _check(st, "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, N))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool = False, workspace=None, stream=None):
+    """Backward: gradients dq, dk, dv (bf16 or fp32, from dq's dtype) of the forward that produced o, lse."""
+    B, H, N, d = q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    grad_fp32 = int(dq.dtype == torch.float32)
+    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
+                      N, d, float(scale), int(bool(causal)), grad_fp32, _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "fa_bwd")
 
 
 def fa_decode_workspace_bytes(B: int, H: int, L: int, d: int, chunk: int = 128, splits: int = 0) -> int:

@@ -173,6 +173,38 @@ fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_
                        void* o, float* lse, int R, int S, int d, void* stream);
 
 /*
+ * fa_bwd_workspace_bytes -- scratch bytes fa_bwd needs: the per-row
+ * D_i = rowsum(O_i * dO_i), B*H*N fp32, rounded up to 256 bytes.  0 for
+ * invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N);
+
+/*
+ * fa_bwd -- attention backward with recomputation: from Q, K, V, the
+ * forward's O and lse, and dO, compute
+ *     D  = rowsum(O * dO),   P = exp(scale Q K^T - lse)  (recomputed per tile),
+ *     dV = P^T dO,   dS = P * (dO V^T - D),   dQ = scale dS K,   dK = scale dS^T Q
+ * (triton-tutorial "8. FlashAttention 实战", §8.8.1-§8.8.4; operatorworld,
+ * "反向传播：用重算换显存").  P is never stored: one kernel owns a key tile
+ * and produces its dK, dV; another owns a query tile and produces its dQ
+ * (no atomics).
+ *
+ *   q, k, v, o, dout  [B, H, N, d] bf16, 16-byte aligned; o and lse must be the
+ *                     forward's outputs for the same q, k, v, scale, causal.
+ *   lse               [B, H, N] fp32 (natural log of scaled scores).
+ *   dq, dk, dv        [B, H, N, d], written: bf16, or fp32 when grad_fp32 = 1.
+ *   d in {64, 128}; scale finite > 0; causal 0/1 as for fa_fwd.
+ *   workspace         >= fa_bwd_workspace_bytes(B, H, N) bytes, 256-byte
+ *                     aligned, caller-owned (holds D); FA_ERR_WORKSPACE if
+ *                     smaller or NULL.
+ * Three kernels run on `stream`: D, then dK/dV, then dQ.
+ */
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, int grad_fp32, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/*
  * fa_get_status -- synchronise `stream`, then read and clear the current
  * device's kernel status word.  Returns FA_ERR_TIMEOUT if any kernel of this
  * library ran out of its wait budget since the last call, FA_ERR_CUDA if the

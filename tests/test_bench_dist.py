@@ -6,27 +6,21 @@ that reduction; the reference arm's non-zero ranks do no work.
 """
 
 import os
-import socket
 import subprocess
 import sys
+import tempfile
 
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
-
-
-def _rank_main(rank, world, port, results):
+def _rank_main(rank, world, store_file, results):
     import torch.distributed as dist
     sys.path.insert(0, ROOT)
     import bench
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # a file rendezvous: no TCP port to race for
+    dist.init_process_group("gloo", init_method=f"file://{store_file}", rank=rank, world_size=world)
     local = [3.5, 7.25][rank]
     results[rank] = bench.max_over_ranks(local, dist)
     dist.barrier()
@@ -37,8 +31,8 @@ def test_slowest_rank_time_is_reported():
     ctx = mp.get_context("spawn")
     manager = ctx.Manager()
     results = manager.dict()
-    port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, results)) for r in range(2)]
+    store_file = os.path.join(tempfile.mkdtemp(), "rendezvous")
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, store_file, results)) for r in range(2)]
     for p in procs:
         p.start()
     for p in procs:

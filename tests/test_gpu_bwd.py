@@ -1,0 +1,90 @@
+"""GPU parity of fa_bwd (gradients with recomputation) against the fp64 oracle.
+
+Tolerance (no page states one for the backward): P~ and dS enter the gradient
+MMAs rounded to bf16 (2^-9 relative) and D is computed from the bf16 O, with
+fp32 accumulation everywhere, so each gradient element carries a few 2^-9 of
+relative error.  The bound: max|g - g_ref| <= 2e-2 * max|g_ref| and
+mean|g - g_ref| <= 1e-2 * mean|g_ref|, per gradient, for fp32 and bf16 outputs.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _util import ensure_built
+from exact_attention_06_gb300 import fattn, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+REL_MAX, REL_MEAN = 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def run_bwd(q, k, v, do, scale, causal, grad_fp32=True):
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=DEV)
+    fattn.fa_fwd(q, k, v, o, lse, scale, causal)
+    dt = torch.float32 if grad_fp32 else torch.bfloat16
+    dq, dk, dv = (torch.full((B, H, N, d), float("nan"), dtype=dt, device=DEV) for _ in range(3))
+    fattn.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal)
+    fattn.fa_get_status()
+    return dq, dk, dv
+
+
+def assert_grads(got, ref, what):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        g = g.double().cpu().numpy()
+        assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
+        e = np.abs(g - r)
+        scale_max, scale_mean = np.abs(r).max(), np.abs(r).mean()
+        if scale_max == 0:
+            assert e.max() <= 1e-5, f"{what} {name}: {e.max():.2e} where the gradient is 0"
+            continue
+        assert e.max() <= REL_MAX * scale_max, f"{what} {name}: max err {e.max():.3e} > {REL_MAX} * {scale_max:.3e}"
+        assert e.mean() <= REL_MEAN * scale_mean, f"{what} {name}: mean err {e.mean():.3e} > {REL_MEAN} * {scale_mean:.3e}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 3, 64, 127, 128, 129, 300, 1000])
+def test_backward_small_and_ragged(n, causal, d):
+    q, k, v = inputs.prefill_inputs(1, 2, n, d, seed=n + 3 * d, device=DEV)
+    do = inputs.normal_bf16((1, 2, n, d), seed=500 + n, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    ref = oracle.attention_backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), scale, causal)
+    assert_grads(run_bwd(q, k, v, do, scale, causal, True), ref, f"N={n} causal={causal} d={d} fp32")
+    assert_grads(run_bwd(q, k, v, do, scale, causal, False), ref, f"N={n} causal={causal} d={d} bf16")
+
+
+def test_backward_spiky_scores():
+    """x8 key spikes (peaked softmax, large alpha jumps in the forward) at N=2048, d=128, causal."""
+    q, k, v = inputs.prefill_inputs(1, 2, 2048, 128, seed=4, device=DEV, spike=True)
+    do = inputs.normal_bf16((1, 2, 2048, 128), seed=41, device=DEV)
+    scale = 1.0 / math.sqrt(128)
+    ref = oracle.attention_backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), scale, True)
+    assert_grads(run_bwd(q, k, v, do, scale, True), ref, "spikes")
+
+
+def test_backward_deterministic_and_identities_at_full_causal_size():
+    """B2 H16 N8192 d128 causal: bitwise repeatable, and sum_keys dV = sum_rows dO, sum_keys dK = 0."""
+    w = inputs.WORKLOADS["causal"]
+    q, k, v = inputs.workload_inputs(w, seed=0, device=DEV)
+    do = inputs.normal_bf16(q.shape, seed=9, device=DEV)
+    g1 = run_bwd(q, k, v, do, w.scale, True)
+    g2 = run_bwd(q, k, v, do, w.scale, True)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    dq, dk, dv = (g.double() for g in g1)
+    sum_dv = dv.sum(dim=2)
+    sum_do = do.double().sum(dim=2)
+    assert float((sum_dv - sum_do).abs().max()) <= 2e-2 * float(sum_do.abs().max())
+    assert float(dk.sum(dim=2).abs().max()) <= 2e-2 * float(dk.abs().sum(dim=2).max())

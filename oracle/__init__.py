@@ -15,6 +15,10 @@ from .attention import (  # noqa: F401
     combine,
     compositions,
     decode,
+    dequantize_blocks,
+    e4m3_values,
     online_attention_head,
     online_merge_scores,
+    quantize_e4m3_blocks,
+    round_to_e4m3,
 )

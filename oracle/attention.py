@@ -34,6 +34,13 @@ What it computes, and where the pages define it
   (triton-tutorial "8. FlashAttention 实战", §8.8.1 gradient formulas and
   §8.8.3 D_i and dS; operatorworld "反向传播：用重算换显存").  P is formed
   explicitly here; the blockwise recomputation from lse is the GPU's business.
+* ``e4m3_values`` / ``quantize_e4m3_blocks`` / ``dequantize_blocks`` -- FP8
+  block quantization (triton-tutorial "8. FlashAttention 实战", §8.9.4: one
+  scale per 128-row block, scale = max|x| / 448, E4M3 max 448): the scale and
+  x / scale are fp32 operations, taken in the kernel's precision because they
+  decide integer codes; the code is the nearest E4M3 value, ties to the even
+  code, saturating at +-448.  The FP8 attention oracle is ``attention`` on the
+  dequantized values.
 * ``chunk_partials`` / ``decode`` -- FlashDecoding split-K: one query row, the
   KV sequence cut into chunks, one partial (U, m, l) per chunk by the plain
   definition restricted to the chunk (cnblogs §三 场景 B, step 2).
@@ -333,4 +340,66 @@ def attention_backward(q, k, v, do, scale: float, causal: bool = False):
 def backward_delta(o, do):
     """D_i = rowsum(O_i * dO_i) (triton-tutorial §8.8.3, the preprocess step)."""
     return (_f64(o) * _f64(do)).sum(axis=-1)
+
+
+def e4m3_values() -> np.ndarray:
+    """The 256 E4M3 (fn variant) codes as fp64: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+    exponent 0 is subnormal (m/8 * 2^-6); code 0x7F/0xFF is NaN (no infinities)."""
+    vals = np.empty(256)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            vals[code] = np.nan
+        elif e == 0:
+            vals[code] = sign * (m / 8.0) * 2.0 ** -6
+        else:
+            vals[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+def round_to_e4m3(x) -> np.ndarray:
+    """Codes (uint8) of the nearest E4M3 values to fp32 x: ties to the even code, |x| > 448 -> +-448,
+    the sign kept (also on zero)."""
+    x = np.asarray(x, dtype=np.float64)
+    vals = e4m3_values()
+    pos_codes = np.arange(0, 0x7F)            # 0 .. 448 (0x7E), ascending values
+    pos_vals = vals[pos_codes]
+    a = np.minimum(np.abs(x), 448.0)
+    idx = np.searchsorted(pos_vals, a)         # first code with value >= a
+    idx = np.clip(idx, 1, len(pos_vals) - 1)
+    lo, hi = pos_vals[idx - 1], pos_vals[idx]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & ((pos_codes[idx] & 1) == 0))
+    code = np.where(pick_hi, pos_codes[idx], pos_codes[idx - 1])
+    code = np.where(a == 0, 0, code)
+    sign = np.signbit(x).astype(np.int64) << 7  # negative values that round to zero give -0 (0x80)
+    return (code | sign).astype(np.uint8)
+
+
+def quantize_e4m3_blocks(x, block: int = 128):
+    """Block quantization of [B, H, N, d] values along N: returns (codes uint8 [B, H, N, d],
+    scales fp32 [B, H, ceil(N/block)]).  scale = amax / 448 in fp32 (1 for an all-zero block) and
+    the code of x / scale (fp32 division) rounded to nearest E4M3."""
+    x32 = np.asarray(_f64(x), dtype=np.float32)
+    b_, h_, n, d = x32.shape
+    nb = -(-n // block)
+    codes = np.zeros(x32.shape, dtype=np.uint8)
+    scales = np.zeros((b_, h_, nb), dtype=np.float32)
+    for b in range(b_):
+        for h in range(h_):
+            for t in range(nb):
+                blk = x32[b, h, t * block:(t + 1) * block]
+                amax = np.float32(np.abs(blk).max())
+                sc = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                scales[b, h, t] = sc
+                codes[b, h, t * block:(t + 1) * block] = round_to_e4m3((blk / sc).astype(np.float32))
+    return codes, scales
+
+
+def dequantize_blocks(codes, scales, block: int = 128):
+    """E4M3 codes [B, H, N, d] and per-block scales -> fp64 values."""
+    vals = e4m3_values()[np.asarray(codes, dtype=np.int64)]
+    sc = np.repeat(np.asarray(scales, dtype=np.float64), block, axis=2)[:, :, :vals.shape[2]]
+    return vals * sc[..., None]
 

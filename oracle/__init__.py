@@ -8,6 +8,8 @@ from .attention import (  # noqa: F401
     admissible_keys,
     attention,
     attention_backward,
+    attention_fp8,
+    attention_fp8_head,
     attention_backward_head,
     attention_head,
     backward_delta,

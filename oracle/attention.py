@@ -39,8 +39,13 @@ What it computes, and where the pages define it
   scale per 128-row block, scale = max|x| / 448, E4M3 max 448): the scale and
   x / scale are fp32 operations, taken in the kernel's precision because they
   decide integer codes; the code is the nearest E4M3 value, ties to the even
-  code, saturating at +-448.  The FP8 attention oracle is ``attention`` on the
-  dequantized values.
+  code, saturating at +-448.
+* ``attention_fp8_head`` / ``attention_fp8`` -- the FP8 forward's mixed
+  precision (triton-tutorial §8.9.3 and §8.9.6): S = (Q8 K8^T) * s_q * s_k *
+  scale, the online softmax of ``online_merge_scores`` in fp64 with l summing
+  the unquantized p, p quantized to E4M3 with a per-block scale before the
+  second GEMM, and U += (P~ V8) * s_p * s_v.  With ``quantize_p=False`` it is
+  ``attention`` on the dequantized values.
 * ``chunk_partials`` / ``decode`` -- FlashDecoding split-K: one query row, the
   KV sequence cut into chunks, one partial (U, m, l) per chunk by the plain
   definition restricted to the chunk (cnblogs §三 场景 B, step 2).
@@ -48,6 +53,10 @@ What it computes, and where the pages define it
 Readings where the pages are silent or disagree (each also listed in the
 design notes):
 * A query row with no admissible key has O = 0 and lse = -inf.
+* FP8: the block scale of P~ for key tile j (the pages leave it open) is
+  s_p = max(s_v) / (256 s_v[j]), so that P~ = E4M3(fp32(p) * 256 s_v[j] / max(s_v))
+  never exceeds 256 (p <= 1) and s_p * s_v[j] = max(s_v) / 256 is the same for
+  every tile.  The code is decided in fp32, as the pages compute p.
 * When the running max is still -inf, 0 is used as the subtraction base so
   that alpha and p are 0 instead of NaN (xuesongtap §2.2: "首个非空块的旧贡献
   系数取 0"; rows that are fully masked skip the invalid exponent difference).
@@ -403,3 +412,76 @@ def dequantize_blocks(codes, scales, block: int = 128):
     sc = np.repeat(np.asarray(scales, dtype=np.float64), block, axis=2)[:, :, :vals.shape[2]]
     return vals * sc[..., None]
 
+
+
+def attention_fp8_head(q8, sq, k8, sk, v8, sv, scale: float, causal: bool = False, rows=None, block: int = 128,
+                       quantize_p: bool = True):
+    """FP8 forward for one head, in the order of triton-tutorial §8.9.3 / §8.9.6.
+
+    q8, k8, v8: [N, d] E4M3 codes; sq, sk, sv: [ceil(N/block)] fp32 block scales (row r of
+    a tensor dequantizes as value(code) * s[r // block]).  Key tiles of ``block`` keys, one
+    per V block, in order; per tile:
+        S     = (Q8 K8_j^T) * s_q[i] * s_k[j] * scale
+        m_new = max(m, rowmax S);  alpha = exp(m - m_new);  p = exp(S - m_new)
+        l     = alpha * l + rowsum(p)                    (the unquantized p)
+        P~    = E4M3(fp32(p) / s_p),  s_p = max(s_v) / (256 s_v[j])
+        U     = alpha * U + (P~ V8_j) * (s_p * s_v[j])
+    then O = U / l and lse = m + log(l).  ``quantize_p=False`` uses p itself in the second
+    GEMM.  Returns (O [R, d], lse [R]) for ``rows`` (default all).
+    """
+    vals = e4m3_values()
+    q8 = np.asarray(q8, dtype=np.int64)
+    k8 = np.asarray(k8, dtype=np.int64)
+    v8 = np.asarray(v8, dtype=np.int64)
+    sq = np.asarray(sq, dtype=np.float32)
+    sk = np.asarray(sk, dtype=np.float32)
+    sv = np.asarray(sv, dtype=np.float32)
+    n, nk = q8.shape[0], k8.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    qv, kv, vv = vals[q8[rows]], vals[k8], vals[v8]
+    s_q = sq[rows // block].astype(np.float64)
+    sv_max = np.float32(sv.max())
+    r = rows.shape[0]
+    m = np.full(r, NEG_INF)
+    l = np.zeros(r)
+    u = np.zeros((r, vv.shape[1]))
+    for j in range(-(-nk // block)):
+        cols = np.arange(j * block, min((j + 1) * block, nk))
+        s = (qv @ kv[cols].T) * (s_q[:, None] * float(sk[j]) * float(scale))
+        if causal:
+            s = np.where(cols[None, :] > rows[:, None], NEG_INF, s)
+        m_new = np.maximum(m, s.max(axis=1))
+        base = np.where(np.isneginf(m_new), 0.0, m_new)  # fully-masked guard
+        alpha = np.exp(m - base)
+        p = np.exp(s - base[:, None])
+        l = alpha * l + p.sum(axis=1)
+        if quantize_p:
+            inv_sp = np.float32(np.float32(256.0) * sv[j]) / sv_max     # 1 / s_p, in fp32
+            p_t = vals[round_to_e4m3(p.astype(np.float32) * inv_sp).astype(np.int64)]
+            s_p = float(sv_max) / (256.0 * float(sv[j]))
+            u = alpha[:, None] * u + (p_t @ vv[cols]) * (s_p * float(sv[j]))
+        else:
+            u = alpha[:, None] * u + p @ (vv[cols] * float(sv[j]))
+        m = m_new
+    safe_l = np.where(l > 0, l, 1.0)
+    o = np.where(l[:, None] > 0, u / safe_l[:, None], 0.0)
+    lse = np.where(l > 0, m + np.log(safe_l), NEG_INF)
+    return o, lse
+
+
+def attention_fp8(q8, sq, k8, sk, v8, sv, scale: float, causal: bool = False, rows=None, block: int = 128,
+                  quantize_p: bool = True):
+    """attention_fp8_head over [B, H, N, d] codes and [B, H, nb] scales; ``rows`` as for ``attention``."""
+    b_, h_, n = q8.shape[0], q8.shape[1], q8.shape[2]
+    r = n if rows is None else np.asarray(rows).shape[-1]
+    out = np.zeros((b_, h_, r, q8.shape[-1]))
+    lse = np.zeros((b_, h_, r))
+    for b in range(b_):
+        for h in range(h_):
+            sel = None
+            if rows is not None:
+                rw = np.asarray(rows, dtype=np.int64)
+                sel = rw if rw.ndim == 1 else rw[b, h]
+            out[b, h], lse[b, h] = attention_fp8_head(q8[b, h], sq[b, h], k8[b, h], sk[b, h], v8[b, h], sv[b, h],
+                                                      scale, causal, sel, block, quantize_p)
+    return out, lse

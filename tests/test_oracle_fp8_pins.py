@@ -54,3 +54,88 @@ def test_block_quantization_round_trip_and_amax():
     blk = x[0, 0, :128]
     i = np.unravel_index(np.abs(blk).argmax(), blk.shape)
     assert abs(oracle.e4m3_values()[codes[0, 0, :128][i]]) == 448.0
+
+
+# ---------------------------------------------------------------- the FP8 forward (attention_fp8)
+
+def _codes(shape, rng, lo=0x20, hi=0x4F):
+    """Random E4M3 codes of either sign with magnitudes between 2^-3 and 3.75."""
+    mag = rng.integers(lo, hi, size=shape)
+    return (mag | (rng.integers(0, 2, size=shape) << 7)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_without_p_quantization_is_sdpa_on_dequantized_inputs(causal):
+    # quantize_p=False reduces the FP8 forward to the plain definition on value(code) * scale;
+    # torch's CPU scaled_dot_product_attention in fp64 is the library routine it must match.
+    rng = np.random.default_rng(11)
+    n, d = 300, 16
+    q8, k8, v8 = (_codes((1, 2, n, d), rng) for _ in range(3))
+    sq, sk, sv = (rng.uniform(0.01, 0.2, size=(1, 2, 3)).astype(np.float32) for _ in range(3))
+    scale = 0.3
+    o, lse = oracle.attention_fp8(q8, sq, k8, sk, v8, sv, scale, causal, quantize_p=False)
+    qd, kd, vd = (torch.from_numpy(oracle.dequantize_blocks(c, s)) for c, s in ((q8, sq), (k8, sk), (v8, sv)))
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, is_causal=causal, scale=scale).numpy()
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+    s = scale * (qd @ kd.transpose(-1, -2))
+    if causal:
+        s = s.masked_fill(torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_uniform_scores_give_the_mean_of_v(causal):
+    # Every key has the same score, so p = 1 for every admissible key and P~ = 256 s_v[j] / max(s_v):
+    # 256 or 128 here, both exact in E4M3.  O is then the mean of the dequantized V rows exactly.
+    rng = np.random.default_rng(12)
+    n, d = 384, 8
+    q8 = _codes((1, 1, n, d), rng)
+    k8 = np.broadcast_to(_codes((1, 1, 1, d), rng), (1, 1, n, d)).copy()
+    v8 = _codes((1, 1, n, d), rng)
+    sq = np.full((1, 1, 3), 0.05, np.float32)
+    sk = np.full((1, 1, 3), 0.07, np.float32)
+    sv = np.array([[[0.25, 0.125, 0.25]]], np.float32)  # ratios 1, 1/2, 1
+    o, lse = oracle.attention_fp8(q8, sq, k8, sk, v8, sv, 1.0, causal)
+    vd = oracle.dequantize_blocks(v8, sv)[0, 0]
+    s = (oracle.dequantize_blocks(q8, sq)[0, 0] @ oracle.dequantize_blocks(k8[:, :, :1], sk[:, :, :1])[0, 0].T)[:, 0]
+    for i in range(n):
+        m = i + 1 if causal else n
+        np.testing.assert_allclose(o[0, 0, i], vd[:m].mean(axis=0), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, 0, i], s[i] + np.log(m), rtol=0, atol=1e-12)
+
+
+def test_fp8_two_keys_half_weight_closed_form():
+    # Two keys whose scores differ by ln 2: p = (1, 1/2), P~ = (256, 128) exactly, so
+    # O = (v0 + v1 / 2) / 1.5 and lse = s0 + ln 1.5.
+    vals = oracle.e4m3_values()
+    q8 = np.array([[[[0x38, 0x00]]]], np.uint8)           # q = (1, 0)
+    k8 = np.array([[[[0x40, 0x00], [0x38, 0x00]]]], np.uint8)  # k0 = (2, 0), k1 = (1, 0): q.k = 2, 1
+    v8 = np.array([[[[0x44, 0xB8], [0x30, 0x48]]]], np.uint8)
+    sq = sk = sv = np.ones((1, 1, 1), np.float32)
+    scale = float(np.log(2.0))
+    o, lse = oracle.attention_fp8(q8, sq, k8, sk, v8, sv, scale)
+    v0, v1 = vals[v8[0, 0, 0].astype(int)], vals[v8[0, 0, 1].astype(int)]
+    np.testing.assert_allclose(o[0, 0, 0], (v0 + v1 / 2) / 1.5, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0, 0], 2 * scale + np.log(1.5), rtol=0, atol=1e-15)
+
+
+def test_fp8_p_quantization_error_within_its_bound():
+    # P~ s_p differs from p by at most half an E4M3 spacing: 2^-4 p for normal codes, 2^-10 s_p
+    # below 2^-6 (subnormal spacing 2^-9).  So per row |O - O_exact| <= sum_k max(2^-4 p_k,
+    # 2^-10 s_p) |v_k| / l with p relative to the running max (<= 1): bounded by
+    # 2^-4 max|v| + n 2^-10 max(s_p) max|v| / l, l >= 1.
+    rng = np.random.default_rng(13)
+    n, d = 520, 32
+    q8, k8, v8 = (_codes((1, 1, n, d), rng) for _ in range(3))
+    sq, sk = (rng.uniform(0.05, 0.1, size=(1, 1, 5)).astype(np.float32) for _ in range(2))
+    sv = rng.uniform(0.1, 0.3, size=(1, 1, 5)).astype(np.float32)
+    for causal in (False, True):
+        o_q, _ = oracle.attention_fp8(q8, sq, k8, sk, v8, sv, 0.5, causal)
+        o_x, lse = oracle.attention_fp8(q8, sq, k8, sk, v8, sv, 0.5, causal, quantize_p=False)
+        vmax = np.abs(oracle.dequantize_blocks(v8, sv)).max()
+        sp_max = sv.max() / (256.0 * sv.min())
+        bound = 2.0 ** -4 * vmax + n * 2.0 ** -10 * sp_max * vmax  # l >= 1 (the max key has p = 1)
+        err = np.abs(o_q - o_x).max()
+        assert 0 < err <= bound + 1e-9
+        # and the error is real: the quantized result is not the exact one
+        assert err > 1e-6

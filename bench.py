@@ -209,6 +209,30 @@ def _backward_step_fn(w, dev, stream):
     return step, 3
 
 
+def _fp8_step_fn(w, dev, stream):
+    """One FP8 forward (fa_fwd_fp8) over the workload; Q, K, V quantized to E4M3 once beforehand
+    (the FP8 path keeps its inputs in HBM as codes plus block scales)."""
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
+    nb = (w.N + 127) // 128
+    packed = []
+    for x in (q, k, v):
+        c = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        s = torch.empty(w.B, w.H, nb, dtype=torch.float32, device=dev)
+        fattn.fa_quantize_e4m3(x, c, s, stream=stream)
+        packed += [c, s]
+    stream.synchronize()
+    del q, k, v
+    (q8, sq, k8, sk, v8, sv) = packed
+    o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+
+    def step():
+        fattn.fa_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, w.scale, w.causal, stream=stream)
+    return step, 1
+
+
 def _time_steps(step, steps, warmup, stream, flush=None, sampler=None, dist_sync=None):
     """Per-step CUDA-event times (ms) of exactly `steps` steps after `warmup` untimed ones."""
     import torch
@@ -237,17 +261,20 @@ def _time_steps(step, steps, warmup, stream, flush=None, sampler=None, dist_sync
 
 
 def _roofline(kind, work_per_launch, launch_ms, peaks, traffic):
-    if kind == "tensor":
+    if kind in ("tensor", "tensor_fp8"):
         achieved = work_per_launch / (launch_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # E4M3 dense rate = the measured bf16 rate x the nominal fp8/bf16 ratio (4.5 / 2.25 PFLOP/s)
+        peak = peaks["bf16_tflops"] * (2.0 if kind == "tensor_fp8" else 1.0)
         unit = "TFLOP/s"
     else:
         achieved = work_per_launch / (launch_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
-    return {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic,
-            "peak_source": f"{peaks['source']} ({'bf16 burst' if kind == 'tensor' else 'copy bandwidth'})"}
+    src = {"tensor": "bf16 burst", "tensor_fp8": "bf16 burst x 2, the nominal fp8/bf16 ratio",
+           "hbm": "copy bandwidth"}[kind]
+    return {"bound": "tensor" if kind == "tensor_fp8" else kind, "achieved": round(achieved, 2), "peak": peak,
+            "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peaks['source']} ({src})"}
 
 
 def _e2e_prefill(w, dev, stream, steps, warmup):
@@ -360,6 +387,19 @@ def run_ours(args):
             "note": "fa_bwd: rowsum(O*dO), dK/dV pass, dQ pass; flops = 2.5 x forward (algorithmic)"}
         del bst
         torch.cuda.empty_cache()
+        # FP8 forward on the causal workload (E4M3 inputs with per-128-row block scales)
+        fst, nl = _fp8_step_fn(wb, dev, stream)
+        fms = _time_steps(fst, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
+        ft = statistics.mean(fms)
+        extra["fp8_causal"] = {
+            "value": round(wb.flops() / (ft * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ft, 4), "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
+            "dtype": "e4m3 (fp32 softmax and accumulation)",
+            "config": {"B": wb.B, "H": wb.H, "N": wb.N, "d": wb.d, "causal": True, "spike_every_64th_key_x8": True},
+            "roofline": _roofline("tensor_fp8", wb.flops(), ft, peaks, _traffic("fwd_kernel_fp8", "causal")),
+            "l2": "inputs larger than L2"}
+        del fst
+        torch.cuda.empty_cache()
 
     e2e = _e2e_prefill(w, dev, stream, max(3, min(args.steps, 50)), max(3, args.warmup))
     if world > 1:
@@ -402,7 +442,8 @@ def run_ours(args):
 
 def run_only(args, w, dev, stream, peaks, flush):
     """One workload alone (profiler captures and sweeps): its step timed like the headline."""
-    fn = _decode_step_fn if w.kind == "decode" else (_backward_step_fn if args.backward else _prefill_step_fn)
+    fn = _decode_step_fn if w.kind == "decode" else (
+        _backward_step_fn if args.backward else (_fp8_step_fn if args.fp8 else _prefill_step_fn))
     step, launches = fn(w, dev, stream)
     small = w.kind == "prefill" and 3 * w.B * w.H * w.N * w.d * 2 < L2_FLUSH_BYTES
     ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush if small else None)
@@ -412,9 +453,11 @@ def run_only(args, w, dev, stream, peaks, flush):
         value = work / (t * 1e-3) / 1e9
     else:
         work = w.flops() * (2.5 if args.backward else 1.0)
-        kind, kern, unit = "tensor", ("bwd" if args.backward else "fwd_kernel"), "TFLOP/s"
+        kind = "tensor_fp8" if args.fp8 else "tensor"
+        kern = "bwd" if args.backward else ("fwd_kernel_fp8" if args.fp8 else "fwd_kernel")
+        unit = "TFLOP/s"
         value = work / (t * 1e-3) / 1e12
-    print(json.dumps({"workload": w.name + (" backward" if args.backward else ""), "value": round(value, 3), "unit": unit, "steps": args.steps,
+    print(json.dumps({"workload": w.name + (" backward" if args.backward else "") + (" fp8" if args.fp8 else ""), "value": round(value, 3), "unit": unit, "steps": args.steps,
                       "warmup": args.warmup, "ms_per_step": round(t, 5), "ms_min": round(min(ms), 5),
                       "gpu_launches": launches * args.steps,
                       "roofline": _roofline(kind, work, t, peaks, _traffic(kern, w.name))}), flush=True)
@@ -520,6 +563,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--only", default=None, help="time one named workload alone (e.g. causal, decode_small)")
     ap.add_argument("--backward", action="store_true", help="with --only: time fa_bwd instead of the forward")
+    ap.add_argument("--fp8", action="store_true", help="with --only: time the FP8 forward (fa_fwd_fp8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

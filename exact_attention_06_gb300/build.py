@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
-SOURCES = ["fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fattn_host.cu"]
+SOURCES = ["fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fa_quant.cu", "fattn_host.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -50,18 +50,22 @@ namespace {
 constexpr int kBr = 128;                 // query rows per tile (TMEM lanes, MMA M)
 constexpr int kBc = 128;                 // keys per tile
 constexpr int kRowsPerCta = 2 * kBr;
-constexpr uint32_t kBox = 128u * 128u;   // bytes of a 128-row x 64-column bf16 box
+constexpr uint32_t kBox = 128u * 128u;   // bytes of a 128-row x 128-byte box (64 bf16 or 128 E4M3 columns)
 constexpr int kSoftmaxWarps = 8;          // per query tile
 constexpr int kWarpMma = 2 * kSoftmaxWarps;  // first MMA warp; also allocates TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+template <int D, bool FP8 = false>
 struct FwdCfg {
-  static constexpr int NH = D / 64;                 // 64-column boxes per row
-  static constexpr int KST = (D == 128) ? 3 : 4;    // K ring stages
-  static constexpr int VST = (D == 128) ? 2 : 4;    // V ring stages
+  static constexpr int ESZ = FP8 ? 1 : 2;           // bytes per element (E4M3 or bf16)
+  static constexpr int ROW = D * ESZ;               // bytes per row
+  static constexpr int NH = ROW / 128;              // 128-byte boxes per row
+  static constexpr int BOX_X = 128 / ESZ;           // elements per box row (TMA x step)
+  static constexpr int K_MMA = 32 / ESZ;            // K elements per MMA instruction (32 bytes)
+  static constexpr int KST = FP8 ? 4 : ((D == 128) ? 3 : 4);  // K ring stages
+  static constexpr int VST = FP8 ? 4 : ((D == 128) ? 2 : 4);  // V ring stages
   static constexpr uint32_t QB = NH * kBox;         // bytes of one Q tile
   static constexpr uint32_t KVB = NH * kBox;        // bytes of one K (or V) tile
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
@@ -69,12 +73,12 @@ struct FwdCfg {
                        NBAR = B_DRAIN + 2;
   // d = 64 leaves 128 TMEM columns free: P~_t gets its own columns there, so S_t(j+1) can be
   // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S.
-  static constexpr bool SEP = (D == 64);
+  static constexpr bool SEP = (D == 64) && !FP8;
   static constexpr uint32_t COL_P = SEP ? 384u : 0u;  // + 64 t (separate) or + 128 t (aliased)
   // At d = 64 the PV MMAs (N = 64) are too short for one issuing thread to keep the tensor core
   // busy, so each tile gets its own MMA warp; at d = 128 one MMA warp alternating between the
   // tiles measured faster.
-  static constexpr bool TWO_ISSUERS = (D == 64);
+  static constexpr bool TWO_ISSUERS = (D == 64) && !FP8;
   static constexpr int WARP_TMA = kWarpMma + (TWO_ISSUERS ? 2 : 1);
   static constexpr int THREADS = (WARP_TMA + 1) * 32;
   static constexpr uint32_t OFF_Q = 0;
@@ -85,6 +89,7 @@ struct FwdCfg {
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;   // + slack to align the base to 1 KB
 };
 static_assert(FwdCfg<128>::SMEM <= 232448, "shared memory of the d=128 kernel exceeds 227 KB");
+static_assert(FwdCfg<128, true>::SMEM <= 232448, "shared memory of the FP8 kernel exceeds 227 KB");
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long budget) {
@@ -127,11 +132,11 @@ __device__ __forceinline__ void rescale_half_row(uint32_t taddr, float alpha) {
 // only rows < N are stored.
 template <int D>
 __device__ __forceinline__ void store_half_row(void* o, float* lse, size_t row_off, int h, bool valid, bool o_fp32,
-                                               uint32_t taddr, float l, float m2) {
+                                               uint32_t taddr, float l, float m2, float o_mult) {
   uint32_t ur[D / 2];
   if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
   if (!valid) return;
-  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  const float inv = (l > 0.f) ? o_mult / l : 0.f;
   if (o_fp32) {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + row_off * D + h * (D / 2));
 #pragma unroll
@@ -153,12 +158,13 @@ __device__ __forceinline__ void store_half_row(void* o, float* lse, size_t row_o
   if (h == 0) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+template <int D, bool CAUSAL, bool FP8>
+__global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, void* __restrict__ o, float* __restrict__ lse, int N,
-               float sl2, int o_fp32, unsigned long long budget) {
-  using C = FwdCfg<D>;
+               float sl2, int o_fp32, unsigned long long budget, const float* __restrict__ sq,
+               const float* __restrict__ sk, const float* __restrict__ sv) {
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -167,6 +173,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const uint32_t sBar = base + C::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  float* sv_max_slot = reinterpret_cast<float*>(gbase + C::OFF_MISC + 8);
 #define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,6 +211,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (FP8) {
+    if (warp == 1) {  // the head's largest V block scale (P~ is quantized relative to it)
+      float mv = 0.f;
+      for (int i = lane; i < n_tiles; i += 32) mv = fmaxf(mv, sv[static_cast<size_t>(bh) * n_tiles + i]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+      if (lane == 0) *sv_max_slot = mv;
+    }
+  }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -222,7 +238,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QB);
       for (int t = 0; t < 2; ++t)
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sQ + t * C::QB + h * kBox, &tq, BAR(C::B_Q), h * 64, pair * kRowsPerCta + t * kBr, bh);
+          tma_load_3d(sQ + t * C::QB + h * kBox, &tq, BAR(C::B_Q), h * C::BOX_X, pair * kRowsPerCta + t * kBr, bh);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_max; ++j) {
         const int ks = j % C::KST;
@@ -231,7 +247,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           break;
         mbar_arrive_expect_tx(BAR(C::B_KF + ks), C::KVB);
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sK + ks * C::KVB + h * kBox, &tk, BAR(C::B_KF + ks), h * 64, j * kBc, bh);
+          tma_load_3d(sK + ks * C::KVB + h * kBox, &tk, BAR(C::B_KF + ks), h * C::BOX_X, j * kBc, bh);
         k_issued = j + 1;
         const int vs = j % C::VST;
         if (j >= C::VST &&
@@ -239,7 +255,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           break;
         mbar_arrive_expect_tx(BAR(C::B_VF + vs), C::KVB);
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sV + vs * C::KVB + h * kBox, &tv, BAR(C::B_VF + vs), h * 64, j * kBc, bh);
+          tma_load_3d(sV + vs * C::KVB + h * kBox, &tv, BAR(C::B_VF + vs), h * C::BOX_X, j * kBc, bh);
         v_issued = j + 1;
       }
       // Every copy this CTA started must land before its shared memory is released.
@@ -333,34 +349,47 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   } else if (!C::TWO_ISSUERS && warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer for both tiles
     if constexpr (!C::TWO_ISSUERS) if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);  // S = Q K^T, both K-major
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);    // U += P V, V is MN-major
+      // S = Q K^T (both K-major); U += P V (V MN-major).  bf16: kind::f16; FP8: kind::f8f6f4, E4M3.
+      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(kBr, kBc, 0) : idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = FP8 ? idesc_e4m3_f32(kBr, D, 1) : idesc_bf16_f32(kBr, D, 1);
       // Descriptors computed once; each MMA below is one 32-bit add plus the tcgen05.mma.
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
+      auto mma_s = [&](bool acc, uint32_t d, uint64_t a, uint64_t b) {
+        if constexpr (FP8) {
+          if (acc) mma_ss_f8_c<1>(d, a, b, idesc_s); else mma_ss_f8_c<0>(d, a, b, idesc_s);
+        } else {
+          if (acc) mma_ss_c<1>(d, a, b, idesc_s); else mma_ss_c<0>(d, a, b, idesc_s);
+        }
+      };
+      auto mma_o = [&](bool acc, uint32_t d, uint32_t a, uint64_t b) {
+        if constexpr (FP8) {
+          if (acc) mma_ts_f8_c<1>(d, a, b, idesc_o); else mma_ts_f8_c<0>(d, a, b, idesc_o);
+        } else {
+          if (acc) mma_ts_c<1>(d, a, b, idesc_o); else mma_ts_c<0>(d, a, b, idesc_o);
+        }
+      };
       auto issue_s = [&](int t, int j) {
         const uint64_t dq = sdesc_add(dq0, t * C::QB);
         const uint64_t dk = sdesc_add(dk0, (j % C::KST) * C::KVB);
         const uint32_t d_s = tmem + t * kBc;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::ROW / 32; ++kk) {  // 32 bytes of K per MMA
           const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
-          if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
-          else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          mma_s(kk > 0, d_s, sdesc_add(dq, off), sdesc_add(dk, off));
         }
       };
       auto issue_pv = [&](int t, int j) {
         const uint64_t dv = sdesc_add(dv0, (j % C::VST) * C::KVB);
         const uint32_t a_p = tmem + (C::SEP ? C::COL_P + 64u * t : static_cast<uint32_t>(t * kBc));
         const uint32_t d_o = tmem + kColO + t * D;
-        // 16 keys per MMA: 16 rows x 128 B of each 64-column V box; boxes kBox apart along d.
-        if (j > 0) mma_ts_c<1>(d_o, a_p, dv, idesc_o);
-        else mma_ts_c<0>(d_o, a_p, dv, idesc_o);
+        // K_MMA keys per MMA: K_MMA rows x 128 B of each V box (boxes kBox apart along d);
+        // the P~ operand advances 8 TMEM columns (32 bytes of each row) per MMA.
 #pragma unroll
-        for (int kk = 1; kk < kBc / 16; ++kk)
-          mma_ts_c<1>(d_o, a_p + static_cast<uint32_t>(kk) * 8u, sdesc_add(dv, static_cast<uint32_t>(kk) * 2048u),
-                      idesc_o);
+        for (int kk = 0; kk < kBc / C::K_MMA; ++kk)
+          mma_o(j > 0 || kk > 0, d_o, a_p + static_cast<uint32_t>(kk) * 8u,
+                sdesc_add(dv, static_cast<uint32_t>(kk * C::K_MMA) * 128u));
       };
       bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, budget, &g_fwd_status) &&
                 mbar_wait(BAR(C::B_KF), 0, abort_flag, budget, &g_fwd_status);
@@ -431,13 +460,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t t_o = tmem + lane_addr + kColO + static_cast<uint32_t>(t * D);
     const uint32_t t_p = tmem + lane_addr + C::COL_P + 64u * t;  // separate P~ columns (d = 64)
     const int lim = CAUSAL ? min(row, N - 1) : N - 1;  // last admissible key of this row
-    const uint64_t c2 = f2_pack(sl2, sl2);
+    const int n_kt = (N + kBc - 1) / kBc;
+    // Q block scale (read only for a tile inside N: the scale array has ceil(N/128) entries per head)
+    const float sq_t = (FP8 && n > 0) ? sq[static_cast<size_t>(bh) * n_kt + pair * 2 + t] : 1.f;
+    const float sv_max = FP8 ? *sv_max_slot : 1.f;
     float m2 = -INFINITY, l = 0.f;  // l: this thread's half of the row
     bool ok = n > 0;
     for (int j = 0; ok && j < n; ++j) {
       ok = wait_all(BAR(C::B_SF + t), j & 1, abort_flag, budget);
       if (!ok) break;
       tc_fence_after();
+      // exponent multiplier of this key tile: scale * log2(e), times the dequantization scales (FP8)
+      const float cj = FP8 ? sq_t * sk[static_cast<size_t>(bh) * n_kt + j] * sl2 : sl2;
+      const uint64_t c2 = f2_pack(cj, cj);
       uint32_t sr[64];
       tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
       if constexpr (C::SEP) {
@@ -463,7 +498,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       a1 = fmax3(a1, __uint_as_float(sr[62]), __uint_as_float(sr[63]));
       float mx = fmax3(a0, a1, fmaxf(a2, a3));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // join the two halves of the row
-      const float m_new = fmaxf(m2, mx * sl2);
+      const float m_new = fmaxf(m2, mx * cj);
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
       const float alpha = ex2(m2 - mb);
       const uint64_t nmb2 = f2_pack(-mb, -mb);
@@ -494,8 +529,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int i = 0; i < 32; ++i) pr[i] = sr[i];
         tmem_st2_x32<32>(t_p, pr);
       }
+      if constexpr (FP8) {
+        // P~ as E4M3 of p * 256 * sv_j / sv_max (<= 256): the V block scale rides on P~ so that
+        // U accumulates in one unit for every key tile; 4 keys per TMEM column.
+        const float ps = 256.f * sv[static_cast<size_t>(bh) * n_kt + j] / sv_max;
+        uint32_t pr[16];
 #pragma unroll
-      for (int q = 0; q < (C::SEP ? 0 : 2); ++q) {
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2, nmb2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2, nmb2), x2,
+                    x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          rs_a = f2_add(rs_a, f2_pack(p0, p1));
+          rs_b = f2_add(rs_b, f2_pack(p2, p3));
+          pr[i] = pack_e4m3x4(p0 * ps, p1 * ps, p2 * ps, p3 * ps);
+        }
+        tmem_st2_x16<16>(t_s, pr);  // keys 64h + 4i .. +3 -> column 16h + i
+      }
+#pragma unroll
+      for (int q = 0; q < ((C::SEP || FP8) ? 0 : 2); ++q) {
         uint32_t pr[16];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
@@ -530,7 +583,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
-      store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2);
+      store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
+                        FP8 ? sv_max * (1.f / 256.f) : 1.f);
     }
     tmem_wait_st();
   }
@@ -543,21 +597,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8 = false>
 cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
-  using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  using C = FwdCfg<D, FP8>;
+  auto kern = fwd_kernel<D, CAUSAL, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   const int n_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget,
+                                              a.sq, a.sk, a.sv);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.fp8) return a.causal ? launch_t<128, true, true>(a, stream) : launch_t<128, false, true>(a, stream);
   if (a.d == 64) return a.causal ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
   return a.causal ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
 }

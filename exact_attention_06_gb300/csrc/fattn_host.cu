@@ -85,18 +85,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A bf16 tensor [batches, rows, d] (d innermost) seen as 3-D {d, rows, batches},
-// loaded in boxes of 64 columns x box_rows rows with 128-byte swizzle.  Rows
-// past `rows` read as zeros.
-fa_status_t make_map(CUtensorMap* map, const void* base, int d, long long rows, long long batches, int box_rows) {
+// A tensor [batches, rows, d] (d innermost) of bf16 (esz = 2) or bytes (esz = 1, E4M3
+// codes) seen as 3-D {d, rows, batches}, loaded in boxes of 128 bytes (64 bf16 or 128
+// E4M3 columns) x box_rows rows with 128-byte swizzle.  Rows past `rows` read as zeros.
+fa_status_t make_map(CUtensorMap* map, const void* base, int d, long long rows, long long batches, int box_rows,
+                     int esz = 2) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(batches)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(rows) * d * esz};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt = esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
@@ -213,6 +215,67 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                    float scale, int causal, void* stream) {
   return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, stream, nullptr);
+}
+
+fa_status_t fa_quantize_e4m3(const void* x, void* codes, float* scales, int B, int H, int N, int d, void* stream) {
+  g_last_error[0] = '\0';
+  if (!x || !codes || !scales) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H and N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (!aligned(x, 16) || !aligned(codes, 16)) return fail(FA_ERR_INVALID_ARG, "x and codes must be 16-byte aligned");
+  if (!aligned(scales, 4)) return fail(FA_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  const long long grid = static_cast<long long>(B) * H * ((N + 127) / 128);
+  if (grid > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H*ceil(N/128)=%lld exceeds the grid limit", grid);
+  fa_status_t st = check_device(nullptr);
+  if (st != FA_OK) return st;
+  cudaGetLastError();
+  cudaError_t e = fattn::launch_quant_e4m3(x, codes, scales, B * H, N, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_quantize_e4m3 launch");
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
+                       const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                       void* stream, const fa_fwd_opts* opts) {
+  g_last_error[0] = '\0';
+  if (!q8 || !k8 || !v8 || !sq || !sk || !sv || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H and N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "the FP8 forward supports d=128 only (got d=%d)", d);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q8, k8, v8 and o must be 16-byte aligned");
+  if (!aligned(lse, 4) || !aligned(sq, 4) || !aligned(sk, 4) || !aligned(sv, 4))
+    return fail(FA_ERR_INVALID_ARG, "lse and the scale arrays must be 4-byte aligned");
+  const int o_fp32 = opts ? opts->o_fp32 : 0;
+  if (o_fp32 != 0 && o_fp32 != 1) return fail(FA_ERR_INVALID_ARG, "opts->o_fp32 must be 0 or 1");
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
+  if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 query-tile grid limit", N);
+  fa_status_t st = check_device(nullptr);
+  if (st != FA_OK) return st;
+
+  fattn::FwdLaunch a{};
+  if ((st = make_map(&a.tq, q8, d, N, bh, 128, 1)) != FA_OK) return st;
+  if ((st = make_map(&a.tk, k8, d, N, bh, 128, 1)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v8, d, N, bh, 128, 1)) != FA_OK) return st;
+  a.o = o;
+  a.lse = lse;
+  a.N = N;
+  a.BH = static_cast<int>(bh);
+  a.d = d;
+  a.causal = causal;
+  a.o_fp32 = o_fp32;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
+  a.fp8 = 1;
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  cudaGetLastError();
+  cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");
+  return FA_OK;
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int L, int d, int chunk, int splits) {

@@ -29,6 +29,10 @@ struct FwdLaunch {
   int o_fp32;
   float scale_log2;  // scale * log2(e)
   unsigned long long budget;
+  int fp8;            // 1: q, k, v are E4M3 with per-128-row block scales sq, sk, sv (d = 128)
+  const float* sq;
+  const float* sk;
+  const float* sv;
 };
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 unsigned int fwd_read_and_clear_status();
@@ -80,6 +84,9 @@ struct BwdLaunch {
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
 unsigned int bwd_read_and_clear_status();
+
+// E4M3 block quantization: x [BH, N, d] bf16 -> codes [BH, N, d] bytes, scales [BH, ceil(N/128)].
+cudaError_t launch_quant_e4m3(const void* x, void* codes, float* scales, int BH, int N, int d, cudaStream_t stream);
 
 // Fixed device scratch used by fa_decode_splitkv_noalloc in place of a
 // caller-provided workspace.  Size limit of that entry point.

@@ -25,7 +25,7 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
             "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_combine", "fa_get_status", "fa_status_string",
             "fa_last_error")
 FA_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -54,6 +54,8 @@ def lib() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
+        L.fa_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
         L.fa_bwd_workspace_bytes.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
@@ -67,7 +69,7 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_decode_splitkv", "fa_decode_splitkv_noalloc",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd", "fa_decode_splitkv", "fa_decode_splitkv_noalloc",
                      "fa_combine", "fa_get_status"):
             getattr(L, name).restype = i
         _lib = L
@@ -122,6 +124,24 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None):
     st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
                       _stream(stream))
     _check(st, "fa_fwd")
+
+
+def fa_quantize_e4m3(x, codes, scales, stream=None):
+    """E4M3 block quantization: x [B, H, N, d] bf16 -> codes [B, H, N, d] uint8, scales [B, H, ceil(N/128)] fp32."""
+    B, H, N, d = x.shape
+    st = lib().fa_quantize_e4m3(_ptr(x), _ptr(codes), _ptr(scales), B, H, N, d, _stream(stream))
+    _check(st, "fa_quantize_e4m3")
+
+
+def fa_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale: float, causal: bool = False, stream=None,
+               wait_budget_cycles: int = 0):
+    """FP8 forward: q8, k8, v8 [B, H, N, 128] uint8 E4M3 codes with block scales sq, sk, sv
+    [B, H, ceil(N/128)] fp32; o [B, H, N, 128] bf16 or fp32 (from its dtype); lse [B, H, N] fp32."""
+    B, H, N, d = q8.shape
+    opts = FaFwdOpts(int(o.dtype == torch.float32), int(wait_budget_cycles))
+    st = lib().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse), B, H, N, d,
+                          float(scale), int(bool(causal)), _stream(stream), ctypes.byref(opts))
+    _check(st, "fa_fwd_fp8")
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:

@@ -84,6 +84,46 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
                       const fa_fwd_opts* opts);
 
 /*
+ * fa_quantize_e4m3 -- block quantization of Q, K or V for fa_fwd_fp8
+ * (triton-tutorial "8. FlashAttention 实战", §8.9.4: one scale per block of
+ * 128 rows x d; scale = max|x| / 448, 448 being E4M3's largest finite value).
+ *
+ *   x        [B, H, N, d] bf16, 16-byte aligned (read).
+ *   codes    [B, H, N, d] bytes, 16-byte aligned (written): the E4M3 code
+ *            (OCP FP8 E4M3, bias 7, no infinities) of x / scale, rounded to
+ *            nearest, ties to even, saturating at +-448; the sign of x is kept.
+ *   scales   [B, H, ceil(N/128)] fp32, 4-byte aligned (written): the block's
+ *            scale, fp32(max|x| / 448), or 1 for an all-zero block.
+ *   B, H, N  >= 1;  d in {64, 128}.
+ * The scale and the division are IEEE fp32 operations, so the codes are a
+ * deterministic function of x.  Returns FA_OK once the kernel is queued.
+ */
+fa_status_t fa_quantize_e4m3(const void* x, void* codes, float* scales,
+                             int B, int H, int N, int d, void* stream);
+
+/*
+ * fa_fwd_fp8 -- fused attention forward on E4M3 inputs (triton-tutorial
+ * §8.9.3: both GEMMs in FP8 with fp32 accumulation, the softmax in fp32,
+ * P quantized to FP8 before the second GEMM).
+ *
+ *   q8, k8, v8  [B, H, N, d] E4M3 codes (fa_quantize_e4m3), 16-byte aligned.
+ *   sq, sk, sv  [B, H, ceil(N/128)] fp32 block scales, 4-byte aligned:
+ *               row r of a head dequantizes as code * s[r / 128].
+ *   o           [B, H, N, d] bf16 (fp32 with opts->o_fp32), 16-byte aligned.
+ *   lse         [B, H, N] fp32 (written), as for fa_fwd.
+ *   d           must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   scale, causal, opts: as for fa_fwd_ex (opts may be NULL).
+ * Scores are S = (q8 k8^T) * sq_i * sk_j * scale in fp32; P~ of key tile j
+ * is stored as E4M3 of p * 256 * sv_j / max_j(sv_j) (p <= 1 after the row
+ * max is subtracted), so that P~ V8 accumulates in one unit for every key
+ * tile and O = U * max(sv) / 256 / l.  l sums the fp32 p.
+ */
+fa_status_t fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                       const float* sq, const float* sk, const float* sv,
+                       void* o, float* lse, int B, int H, int N, int d, float scale,
+                       int causal, void* stream, const fa_fwd_opts* opts);
+
+/*
  * fa_decode_workspace_bytes -- bytes of scratch that fa_decode_splitkv needs.
  *
  * The workspace holds one partial (U [d] fp32, m fp32, l fp32) per (b, h, split).

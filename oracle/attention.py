@@ -415,7 +415,7 @@ def dequantize_blocks(codes, scales, block: int = 128):
 
 
 def attention_fp8_head(q8, sq, k8, sk, v8, sv, scale: float, causal: bool = False, rows=None, block: int = 128,
-                       quantize_p: bool = True):
+                       quantize_p: bool = True, trace: list | None = None):
     """FP8 forward for one head, in the order of triton-tutorial §8.9.3 / §8.9.6.
 
     q8, k8, v8: [N, d] E4M3 codes; sq, sk, sv: [ceil(N/block)] fp32 block scales (row r of
@@ -427,7 +427,9 @@ def attention_fp8_head(q8, sq, k8, sk, v8, sv, scale: float, causal: bool = Fals
         P~    = E4M3(fp32(p) / s_p),  s_p = max(s_v) / (256 s_v[j])
         U     = alpha * U + (P~ V8_j) * (s_p * s_v[j])
     then O = U / l and lse = m + log(l).  ``quantize_p=False`` uses p itself in the second
-    GEMM.  Returns (O [R, d], lse [R]) for ``rows`` (default all).
+    GEMM.  Returns (O [R, d], lse [R]) for ``rows`` (default all).  When ``trace`` is a list,
+    one dict per key tile is appended: its key indices ``cols``, the fp32 values ``x`` that
+    are rounded to P~ codes, and the running max ``m`` after the tile.
     """
     vals = e4m3_values()
     q8 = np.asarray(q8, dtype=np.int64)
@@ -457,7 +459,10 @@ def attention_fp8_head(q8, sq, k8, sk, v8, sv, scale: float, causal: bool = Fals
         l = alpha * l + p.sum(axis=1)
         if quantize_p:
             inv_sp = np.float32(np.float32(256.0) * sv[j]) / sv_max     # 1 / s_p, in fp32
-            p_t = vals[round_to_e4m3(p.astype(np.float32) * inv_sp).astype(np.int64)]
+            x = p.astype(np.float32) * inv_sp
+            if trace is not None:
+                trace.append({"cols": cols, "x": x, "m": m_new.copy()})
+            p_t = vals[round_to_e4m3(x).astype(np.int64)]
             s_p = float(sv_max) / (256.0 * float(sv[j]))
             u = alpha[:, None] * u + (p_t @ vv[cols]) * (s_p * float(sv[j]))
         else:

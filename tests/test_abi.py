@@ -28,7 +28,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for n in ("fa_fwd", "fa_fwd_ex", "fa_decode_splitkv", "fa_decode_workspace_bytes", "fa_combine",
+    for n in ("fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_quantize_e4m3", "fa_decode_splitkv",
+              "fa_decode_workspace_bytes", "fa_combine",
               "fa_get_status", "fa_status_string", "fa_last_error"):
         assert n in names
 
@@ -96,3 +97,24 @@ def test_decode_and_combine_argument_checks_need_no_gpu(lib):
     assert st == fattn.FA_ERR_INVALID_ARG
     st = lib.fa_combine(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 2, 32, vp(0))
     assert st == fattn.FA_ERR_UNSUPPORTED
+
+
+def test_fp8_argument_checks_need_no_gpu(lib):
+    from exact_attention_06_gb300 import fattn
+    vp, f = ctypes.c_void_p, ctypes.c_float
+
+    def fwd8(ptrs=(16,) * 8, N=256, d=128, scale=0.1, causal=0):
+        return lib.fa_fwd_fp8(*(vp(p) for p in ptrs), 1, 2, N, d, f(scale), causal, vp(0), None)
+
+    assert fwd8(d=64) == fattn.FA_ERR_UNSUPPORTED  # FP8 forward is d = 128 only
+    assert fwd8(ptrs=(16, 16, 16, 0, 16, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # null scale array
+    assert fwd8(ptrs=(16, 16, 8, 16, 16, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # misaligned v8
+    assert fwd8(ptrs=(16, 16, 16, 16, 18, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # misaligned sk
+    assert fwd8(N=0) == fattn.FA_ERR_INVALID_ARG
+    assert fwd8(scale=-1.0) == fattn.FA_ERR_INVALID_ARG
+    assert fwd8(causal=3) == fattn.FA_ERR_INVALID_ARG
+    q = lib.fa_quantize_e4m3
+    assert q(vp(16), vp(16), vp(16), 1, 1, 128, 96, vp(0)) == fattn.FA_ERR_UNSUPPORTED
+    assert q(vp(16), vp(24), vp(16), 1, 1, 128, 128, vp(0)) == fattn.FA_ERR_INVALID_ARG  # codes misaligned
+    assert q(vp(16), vp(16), vp(0), 1, 1, 128, 128, vp(0)) == fattn.FA_ERR_INVALID_ARG
+    assert q(vp(16), vp(16), vp(16), 1, 0, 128, 128, vp(0)) == fattn.FA_ERR_INVALID_ARG

@@ -17,6 +17,8 @@ from .attention import (  # noqa: F401
     combine,
     compositions,
     decode,
+    decode_paged,
+    paged_rows,
     dequantize_blocks,
     e4m3_values,
     online_attention_head,

@@ -46,6 +46,11 @@ What it computes, and where the pages define it
   the unquantized p, p quantized to E4M3 with a per-block scale before the
   second GEMM, and U += (P~ V8) * s_p * s_v.  With ``quantize_p=False`` it is
   ``attention`` on the dequantized values.
+* ``paged_rows`` / ``decode_paged`` -- decode over a paged KV cache: key j of
+  sequence b is row j % page_size of pool page block_table[b][j // page_size]
+  (iceferryling §13 names the paged block table; the layout [P, H, page_size,
+  d] and "an id outside the pool reads as zeros" are this library's reading),
+  then the decode definition over seq_lens[b] keys.
 * ``chunk_partials`` / ``decode`` -- FlashDecoding split-K: one query row, the
   KV sequence cut into chunks, one partial (U, m, l) per chunk by the plain
   definition restricted to the chunk (cnblogs §三 场景 B, step 2).
@@ -301,6 +306,42 @@ def decode(q, k, v, scale: float, pairs=None):
     lse = np.zeros(len(pairs))
     for idx, (b, h) in enumerate(pairs):
         o, ls = attention_head(_f64(q[b, h])[None, :], _f64(k[b, h]), _f64(v[b, h]), scale, False)
+        out[idx], lse[idx] = o[0], ls[0]
+    return out, lse
+
+
+def paged_rows(pages, block_table, b: int, h: int, n_keys: int) -> np.ndarray:
+    """Rows 0 .. n_keys-1 of sequence b, head h, read from a paged pool [P, H, page_size, d]:
+    key j sits in row j % page_size of pool page block_table[b][j // page_size]; a page id
+    outside [0, P) reads as zeros."""
+    pages = _f64(pages)
+    n_pages, _, page_size, d = pages.shape
+    out = np.zeros((n_keys, d))
+    for j in range(0, n_keys, page_size):
+        pid = int(block_table[b][j // page_size])
+        m = min(page_size, n_keys - j)
+        if 0 <= pid < n_pages:
+            out[j:j + m] = pages[pid, h, :m]
+    return out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale: float, pairs=None):
+    """Decode over a paged KV cache (iceferryling §13, paged block table): sequence b has
+    seq_lens[b] keys, gathered through ``paged_rows``; then ``decode``'s plain definition.
+    q [B, H, d] -> O [P, dv], lse [P] for ``pairs`` (default every (b, h))."""
+    b_, h_ = q.shape[0], q.shape[1]
+    if pairs is None:
+        pairs = [(b, h) for b in range(b_) for h in range(h_)]
+    pairs = [(int(b), int(h)) for b, h in pairs]
+    table = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    out = np.zeros((len(pairs), _f64(v_pages).shape[-1]))
+    lse = np.zeros(len(pairs))
+    for idx, (b, h) in enumerate(pairs):
+        n = max(int(lens[b]), 0)
+        kb = paged_rows(k_pages, table, b, h, n)
+        vb = paged_rows(v_pages, table, b, h, n)
+        o, ls = attention_head(_f64(q[b, h])[None, :], kb, vb, scale, False)
         out[idx], lse[idx] = o[0], ls[0]
     return out, lse
 

@@ -209,6 +209,34 @@ def _backward_step_fn(w, dev, stream):
     return step, 3
 
 
+def _paged_decode_step_fn(w, dev, stream, page_size=128):
+    """Split-KV decode over a paged cache: the workload's K/V written into pools of 128-key pages
+    in a seeded random order, every sequence at full length."""
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
+    n = -(-w.N // page_size)
+    assert w.N == n * page_size
+    perm = torch.randperm(w.B * n, generator=torch.Generator().manual_seed(3)).to(dev)
+    table = perm.view(w.B, n).to(torch.int32)
+    pools = []
+    for x in (k, v):
+        pool = torch.empty((w.B * n, w.H, page_size, w.d), dtype=torch.bfloat16, device=dev)
+        pool[perm] = x.view(w.B, w.H, n, page_size, w.d).permute(0, 2, 1, 3, 4).reshape(w.B * n, w.H, page_size, w.d)
+        pools.append(pool)
+    del k, v, x
+    kp, vp = pools
+    lens = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+    o = torch.empty(w.B, w.H, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(fattn.fa_decode_paged_workspace_bytes(w.B, w.H, w.N, w.d, page_size, n, 0), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        fattn.fa_decode_paged(q, kp, vp, table, lens, o, lse, w.scale, w.N, workspace=ws, stream=stream)
+    return step, 2
+
+
 def _fp8_step_fn(w, dev, stream):
     """One FP8 forward (fa_fwd_fp8) over the workload; Q, K, V quantized to E4M3 once beforehand
     (the FP8 path keeps its inputs in HBM as codes plus block scales)."""
@@ -387,6 +415,19 @@ def run_ours(args):
             "note": "fa_bwd: rowsum(O*dO), dK/dV pass, dQ pass; flops = 2.5 x forward (algorithmic)"}
         del bst
         torch.cuda.empty_cache()
+        # split-KV decode over a paged cache (128-key pages, shuffled pool) on the decode workload
+        wd = inputs.WORKLOADS["decode"]
+        pst, nl = _paged_decode_step_fn(wd, dev, stream)
+        pms = _time_steps(pst, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
+        pt = statistics.mean(pms)
+        extra["decode_paged"] = {
+            "value": round(wd.kv_bytes() / (pt * 1e-3) / 1e9 * world, 3), "unit": "GB/s",
+            "ms_per_step": round(pt, 4), "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
+            "config": {"B": wd.B, "H": wd.H, "L": wd.N, "d": wd.d, "page_size": 128, "pool": "shuffled pages"},
+            "roofline": _roofline("hbm", wd.kv_bytes(), pt, peaks, None),
+            "note": "fa_decode_paged: split kernel through the block table, then the combine kernel"}
+        del pst
+        torch.cuda.empty_cache()
         # FP8 forward on the causal workload (E4M3 inputs with per-128-row block scales)
         fst, nl = _fp8_step_fn(wb, dev, stream)
         fms = _time_steps(fst, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
@@ -442,7 +483,7 @@ def run_ours(args):
 
 def run_only(args, w, dev, stream, peaks, flush):
     """One workload alone (profiler captures and sweeps): its step timed like the headline."""
-    fn = _decode_step_fn if w.kind == "decode" else (
+    fn = (_paged_decode_step_fn if args.paged else _decode_step_fn) if w.kind == "decode" else (
         _backward_step_fn if args.backward else (_fp8_step_fn if args.fp8 else _prefill_step_fn))
     step, launches = fn(w, dev, stream)
     small = w.kind == "prefill" and 3 * w.B * w.H * w.N * w.d * 2 < L2_FLUSH_BYTES
@@ -457,7 +498,8 @@ def run_only(args, w, dev, stream, peaks, flush):
         kern = "bwd" if args.backward else ("fwd_kernel_fp8" if args.fp8 else "fwd_kernel")
         unit = "TFLOP/s"
         value = work / (t * 1e-3) / 1e12
-    print(json.dumps({"workload": w.name + (" backward" if args.backward else "") + (" fp8" if args.fp8 else ""), "value": round(value, 3), "unit": unit, "steps": args.steps,
+    tag = (" backward" if args.backward else "") + (" fp8" if args.fp8 else "") + (" paged" if args.paged else "")
+    print(json.dumps({"workload": w.name + tag, "value": round(value, 3), "unit": unit, "steps": args.steps,
                       "warmup": args.warmup, "ms_per_step": round(t, 5), "ms_min": round(min(ms), 5),
                       "gpu_launches": launches * args.steps,
                       "roofline": _roofline(kind, work, t, peaks, _traffic(kern, w.name))}), flush=True)
@@ -564,6 +606,7 @@ def main():
     ap.add_argument("--only", default=None, help="time one named workload alone (e.g. causal, decode_small)")
     ap.add_argument("--backward", action="store_true", help="with --only: time fa_bwd instead of the forward")
     ap.add_argument("--fp8", action="store_true", help="with --only: time the FP8 forward (fa_fwd_fp8)")
+    ap.add_argument("--paged", action="store_true", help="with --only and a decode workload: time fa_decode_paged")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

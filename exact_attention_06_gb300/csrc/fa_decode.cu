@@ -20,6 +20,15 @@
 //           (32/(d/8))-th key; p comes from the owning lane by shuffle.
 // Each warp keeps its own (m, l, U); the four are merged through shared
 // memory at the end with the same rule as the combine kernel.
+//
+// Paged KV cache (iceferryling §13: decode kernels read the cache through a
+// paged block table): K and V live in pools of pages [P, H, page_size, d];
+// sequence b's logical page i is pool page block_table[b][i], and its length
+// is seq_lens[b].  The split kernel then copies the split's page ids into
+// shared memory once and points each 64-key TMA tile at (page * H + head,
+// key % page_size); a page id outside [0, P) reads as zero rows (the TMA
+// out-of-bounds fill).  Keys at or past seq_lens[b] are masked and their V
+// rows skipped, so whatever a partly filled page holds there never reaches O.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -51,7 +60,9 @@ struct DecCfg {
   static constexpr uint32_t OFF_BAR = 2 * kSt * TB;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;       // abort flag
   static constexpr uint32_t OFF_RED = OFF_MISC + 16u;              // m_w[kNw], l_w[kNw], U_w[kNw][D]
-  static constexpr uint32_t SMEM = OFF_RED + 4u * (2 * kNw + kNw * D) + 1024u;
+  static constexpr uint32_t OFF_PAGES = OFF_RED + 4u * (2 * kNw + kNw * D);  // paged: the split's page ids
+  static constexpr uint32_t SMEM = OFF_PAGES + 1024u;
+  static constexpr uint32_t SMEM_PAGED = OFF_PAGES + 4u * kMaxSplitPages + 1024u;
 };
 
 __device__ __forceinline__ bool dwait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -84,12 +95,18 @@ __device__ __forceinline__ float dot8(const uint4& x, const float* q, float acc)
   return acc;
 }
 
-template <int D>
+struct PagedArgs {
+  const int* block_table;  // [B, max_pages]
+  const int* seq_lens;     // [B]
+  int H, page_size, max_pages, num_pages;
+};
+
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads)
     decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                         const __nv_bfloat16* __restrict__ q, float* __restrict__ u_part, float* __restrict__ m_part,
                         float* __restrict__ l_part, int L, int splits, int keys_per_split, float sl2,
-                        unsigned long long budget) {
+                        unsigned long long budget, const PagedArgs pg) {
   using C = DecCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -103,10 +120,27 @@ __global__ void __launch_bounds__(kThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(splits));
   const int sp = static_cast<int>(blockIdx.x % static_cast<unsigned>(splits));
+  int* page_ids = reinterpret_cast<int*>(gbase + C::OFF_PAGES);
+  int Lr = L;  // keys of this row
+  int b = 0, head = 0;
+  if constexpr (PAGED) {
+    b = bh / pg.H;
+    head = bh - b * pg.H;
+    Lr = min(max(pg.seq_lens[b], 0), L);  // L = the longest sequence the caller planned for
+  }
   const long long k0ll = static_cast<long long>(sp) * keys_per_split;
-  const int k0 = static_cast<int>(k0ll < L ? k0ll : L);
-  const int k1 = static_cast<int>(k0ll + keys_per_split < L ? k0ll + keys_per_split : L);
+  const int k0 = static_cast<int>(k0ll < Lr ? k0ll : Lr);
+  const int k1 = static_cast<int>(k0ll + keys_per_split < Lr ? k0ll + keys_per_split : Lr);
   const int n_st = (k1 - k0 + kSk - 1) / kSk;
+  if constexpr (PAGED) {
+    // pool page of each logical page this split touches (the host keeps the count <= kMaxSplitPages)
+    const int pg0 = k0 / pg.page_size;
+    const int npg = k1 > k0 ? (k1 - 1) / pg.page_size - pg0 + 1 : 0;
+    for (int i = threadIdx.x; i < npg; i += kThreads) {
+      const int id = pg.block_table[static_cast<size_t>(b) * pg.max_pages + pg0 + i];
+      page_ids[i] = (id >= 0 && id < pg.num_pages) ? id * pg.H + head : -1;  // -1: outside the pool, reads zeros
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSt; ++s) {
@@ -131,10 +165,15 @@ __global__ void __launch_bounds__(kThreads)
             !mbar_wait(BAR(C::B_EMPTY + s), ((st / kSt) - 1) & 1, abort_flag, budget, &g_dec_status))
           break;
         const int key = k0 + st * kSk;
+        int row = key, z = bh;  // contiguous cache: tensor [BH, L, d]
+        if constexpr (PAGED) {  // pool [P * H, page_size, d]; a 64-key stage never straddles a page
+          row = key % pg.page_size;
+          z = page_ids[key / pg.page_size - k0 / pg.page_size];
+        }
         mbar_arrive_expect_tx(BAR(C::B_KF + s), C::TB);
-        for (int h = 0; h < C::NH; ++h) tma_load_3d(sK + s * C::TB + h * C::BOX, &tk, BAR(C::B_KF + s), h * 64, key, bh);
+        for (int h = 0; h < C::NH; ++h) tma_load_3d(sK + s * C::TB + h * C::BOX, &tk, BAR(C::B_KF + s), h * 64, row, z);
         mbar_arrive_expect_tx(BAR(C::B_VF + s), C::TB);
-        for (int h = 0; h < C::NH; ++h) tma_load_3d(sV + s * C::TB + h * C::BOX, &tv, BAR(C::B_VF + s), h * 64, key, bh);
+        for (int h = 0; h < C::NH; ++h) tma_load_3d(sV + s * C::TB + h * C::BOX, &tv, BAR(C::B_VF + s), h * 64, row, z);
         issued = st + 1;
       }
       for (int st = issued - kSt < 0 ? 0 : issued - kSt; st < issued; ++st) {
@@ -210,6 +249,8 @@ __global__ void __launch_bounds__(kThreads)
         const int r = kg + i * KG;  // key within this warp's 16
         const float pk = __shfl_sync(0xffffffffu, p, r);
         const int vk = warp * 16 + r;
+        // paged: rows past the sequence hold whatever the page holds; they must not reach U (0 * NaN)
+        if (PAGED && k0 + st * kSk + vk >= k1) continue;
         const uint4 x = lds128(vb + vk * 128 + (((dc & 7) ^ (vk & 7)) << 4));
         u[0] = fmaf(pk, bf16lo(x.x), u[0]);
         u[1] = fmaf(pk, bf16hi(x.x), u[1]);
@@ -290,22 +331,25 @@ __global__ void __launch_bounds__(D)
   if (t == 0) lse[r] = lt > 0.f ? mm + logf(lt) : -INFINITY;
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_split_t(const DecodeLaunch& a, cudaStream_t stream) {
   using C = DecCfg<D>;
-  auto kern = decode_split_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  auto kern = decode_split_kernel<D, PAGED>;
+  const uint32_t smem = PAGED ? C::SMEM_PAGED : C::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(static_cast<long long>(a.BH) * a.splits);
-  kern<<<grid, kThreads, C::SMEM, stream>>>(a.tk, a.tv, static_cast<const __nv_bfloat16*>(a.q), a.u_part, a.m_part,
-                                            a.l_part, a.L, a.splits, a.keys_per_split, a.scale_log2, a.budget);
+  const PagedArgs pg{a.block_table, a.seq_lens, a.H, a.page_size, a.max_pages, a.num_pages};
+  kern<<<grid, kThreads, smem, stream>>>(a.tk, a.tv, static_cast<const __nv_bfloat16*>(a.q), a.u_part, a.m_part,
+                                         a.l_part, a.L, a.splits, a.keys_per_split, a.scale_log2, a.budget, pg);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_split(const DecodeLaunch& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_split_t<64>(a, stream) : launch_split_t<128>(a, stream);
+  if (a.block_table) return a.d == 64 ? launch_split_t<64, true>(a, stream) : launch_split_t<128, true>(a, stream);
+  return a.d == 64 ? launch_split_t<64, false>(a, stream) : launch_split_t<128, false>(a, stream);
 }
 
 cudaError_t launch_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,

@@ -155,6 +155,37 @@ fa_status_t plan_decode(int B, int H, int L, int d, int chunk, int splits, int s
   return FA_OK;
 }
 
+
+// Splits for the paged decode: as for the contiguous cache, then raised if a split would
+// touch more than kMaxSplitPages pages (only for very long sequences with small pages).
+fa_status_t plan_paged(int B, int H, int L, int d, int page_size, int splits, int sms, DecodePlan* plan) {
+  fa_status_t st = plan_decode(B, H, L, d, 128, splits, sms, plan);
+  if (st != FA_OK) return st;
+  auto pages_of = [&](const DecodePlan& p) { return p.keys_per_split / page_size + 1; };
+  if (pages_of(*plan) <= fattn::kMaxSplitPages) return FA_OK;
+  if (splits != 0)
+    return fail(FA_ERR_UNSUPPORTED, "splits=%d gives %d keys per split, more than %d pages of %d keys", splits,
+                plan->keys_per_split, fattn::kMaxSplitPages - 1, page_size);
+  const int n_chunks = (L + 127) / 128;
+  const int chunks_per_split = ((fattn::kMaxSplitPages - 1) * page_size) / 128;
+  return plan_decode(B, H, L, d, 128, (n_chunks + chunks_per_split - 1) / chunks_per_split, 0, plan);
+}
+
+fa_status_t check_paged_args(int B, int H, int d, int page_size, int max_pages, int num_pages, int max_seq_len) {
+  if (B < 1 || H < 1) return fail(FA_ERR_INVALID_ARG, "B and H must be >= 1 (got %d, %d)", B, H);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (page_size < 64 || page_size % 64 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "page_size=%d must be a positive multiple of 64", page_size);
+  if (max_pages < 1 || num_pages < 1)
+    return fail(FA_ERR_INVALID_ARG, "max_pages and num_pages must be >= 1 (got %d, %d)", max_pages, num_pages);
+  if (max_seq_len < 1 || static_cast<long long>(max_seq_len) > static_cast<long long>(max_pages) * page_size)
+    return fail(FA_ERR_INVALID_ARG, "max_seq_len=%d must be in [1, max_pages * page_size]", max_seq_len);
+  if (static_cast<long long>(num_pages) * H > INT_MAX)
+    return fail(FA_ERR_UNSUPPORTED, "num_pages*H=%lld exceeds the page index range",
+                static_cast<long long>(num_pages) * H);
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -368,6 +399,84 @@ fa_status_t fa_decode_splitkv_noalloc(const void* q, const void* k, const void* 
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_noalloc scratch address");
   return fa_decode_splitkv(q, k, v, o, lse, B, H, L, d, scale, chunk, plan.splits, scratch,
                            fattn::kNoAllocScratchBytes, stream);
+}
+
+
+size_t fa_decode_paged_workspace_bytes(int B, int H, int max_seq_len, int d, int page_size, int max_pages,
+                                       int splits) {
+  const int saved = g_last_error[0];
+  DecodePlan plan;
+  fa_status_t st = check_paged_args(B, H, d, page_size, max_pages, 1, max_seq_len);
+  int sms = 0;
+  if (st == FA_OK && splits == 0) st = check_device(&sms);
+  if (st == FA_OK) st = plan_paged(B, H, max_seq_len, d, page_size, splits, sms, &plan);
+  if (!saved) g_last_error[0] = '\0';
+  return st == FA_OK ? plan.total() : 0;
+}
+
+fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                            const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size,
+                            int max_pages, int num_pages, int max_seq_len, float scale, int splits, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o || !lse)
+    return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k_pages, v_pages and o must be 16-byte aligned");
+  if (!aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(FA_ERR_INVALID_ARG, "lse, block_table and seq_lens must be 4-byte aligned");
+  if (workspace && !aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  fa_status_t st = check_paged_args(B, H, d, page_size, max_pages, num_pages, max_seq_len);
+  if (st != FA_OK) return st;
+  if (splits < 0) return fail(FA_ERR_INVALID_ARG, "splits=%d must be >= 0", splits);
+  DecodePlan plan;
+  int sms = 0;
+  if (splits != 0) {
+    if ((st = plan_paged(B, H, max_seq_len, d, page_size, splits, 0, &plan)) != FA_OK) return st;
+    if (!workspace || ws_bytes < plan.total())
+      return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes,
+                  plan.total());
+    if ((st = check_device(nullptr)) != FA_OK) return st;
+  } else {
+    if ((st = check_device(&sms)) != FA_OK) return st;
+    if ((st = plan_paged(B, H, max_seq_len, d, page_size, 0, sms, &plan)) != FA_OK) return st;
+  }
+  if (!workspace || ws_bytes < plan.total())
+    return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes,
+                plan.total());
+  const long long bh = static_cast<long long>(B) * H;
+  fattn::DecodeLaunch a{};
+  const long long planes = static_cast<long long>(num_pages) * H;
+  if ((st = make_map(&a.tk, k_pages, d, page_size, planes, fattn::kDecodeStageKeys)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v_pages, d, page_size, planes, fattn::kDecodeStageKeys)) != FA_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  a.q = q;
+  a.u_part = reinterpret_cast<float*>(ws);
+  a.m_part = reinterpret_cast<float*>(ws + plan.u_bytes);
+  a.l_part = reinterpret_cast<float*>(ws + plan.u_bytes + plan.m_bytes);
+  a.o = o;
+  a.lse = lse;
+  a.L = max_seq_len;
+  a.BH = static_cast<int>(bh);
+  a.d = d;
+  a.splits = plan.splits;
+  a.keys_per_split = plan.keys_per_split;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.budget = kDefaultBudget;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.H = H;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fattn::launch_decode_split(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged split launch");
+  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged combine launch");
+  return FA_OK;
 }
 
 fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,

@@ -54,8 +54,13 @@ struct DecodeLaunch {
   int keys_per_split;  // multiple of 128
   float scale_log2;
   unsigned long long budget;
+  // paged KV cache (block_table != nullptr): tk/tv map pools [P * H, page_size, d]
+  const int* block_table;  // [B, max_pages]
+  const int* seq_lens;     // [B]; L above is the longest length planned for
+  int H, page_size, max_pages, num_pages;
 };
 constexpr int kDecodeStageKeys = 64;  // keys per pipeline stage of the split kernel
+constexpr int kMaxSplitPages = 1024;  // page ids one split of the paged decode may touch
 constexpr int kDecodeCtasPerSm = 2;   // resident split CTAs per SM (shared-memory bound)
 cudaError_t launch_decode_split(const DecodeLaunch& a, cudaStream_t stream);
 cudaError_t launch_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse,

@@ -26,7 +26,8 @@ FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
-            "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_combine", "fa_get_status", "fa_status_string",
+            "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes", "fa_decode_paged",
+            "fa_combine", "fa_get_status", "fa_status_string",
             "fa_last_error")
 FA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -63,13 +64,17 @@ def lib() -> ctypes.CDLL:
         L.fa_decode_workspace_bytes.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
         L.fa_decode_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        L.fa_decode_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        L.fa_decode_paged_workspace_bytes.restype = sz
+        L.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
         L.fa_combine.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
         L.fa_get_status.argtypes = [vp]
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd", "fa_decode_splitkv", "fa_decode_splitkv_noalloc",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd", "fa_decode_splitkv",
+                     "fa_decode_splitkv_noalloc", "fa_decode_paged",
                      "fa_combine", "fa_get_status"):
             getattr(L, name).restype = i
         _lib = L
@@ -184,6 +189,28 @@ def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, chunk: int = 128, s
     st = lib().fa_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale),
                                          chunk, splits, _stream(stream))
     _check(st, "fa_decode_splitkv_noalloc")
+
+
+def fa_decode_paged_workspace_bytes(B: int, H: int, max_seq_len: int, d: int, page_size: int, max_pages: int,
+                                    splits: int = 0) -> int:
+    return int(lib().fa_decode_paged_workspace_bytes(B, H, max_seq_len, d, page_size, max_pages, splits))
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale: float, max_seq_len: int,
+                    workspace=None, splits: int = 0, stream=None):
+    """Split-KV decode over a paged cache: q [B, H, d]; k_pages/v_pages [P, H, page_size, d];
+    block_table [B, max_pages] int32; seq_lens [B] int32; o [B, H, d] bf16; lse [B, H] fp32."""
+    B, H, d = q.shape
+    P, _, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    if workspace is None:
+        workspace = torch.empty(fa_decode_paged_workspace_bytes(B, H, max_seq_len, d, page_size, max_pages, splits),
+                                dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o),
+                               _ptr(lse), B, H, d, page_size, max_pages, P, max_seq_len, float(scale), splits,
+                               _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "fa_decode_paged")
 
 
 def fa_combine(u_part, m_part, l_part, o, lse, stream=None):

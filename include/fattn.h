@@ -195,6 +195,43 @@ fa_status_t fa_decode_splitkv_noalloc(const void* q, const void* k, const void* 
                                       void* stream);
 
 /*
+ * fa_decode_paged -- fa_decode_splitkv over a paged KV cache (iceferryling
+ * "FlashAttention 1 和 FlashAttention 2 的区别", §13: decode kernels read the
+ * cache through a paged block table).  Same split and combine; only the
+ * address of each key changes.
+ *
+ *   q            [B, H, d] bf16, 16-byte aligned.
+ *   k_pages,     [num_pages, H, page_size, d] bf16 pools, 16-byte aligned:
+ *   v_pages      page p holds page_size consecutive keys of one sequence for
+ *                every head.
+ *   block_table  [B, max_pages] int32, 4-byte aligned: logical page i of
+ *                sequence b (keys i*page_size .. +page_size-1) is pool page
+ *                block_table[b*max_pages + i].  Only the entries covering
+ *                seq_lens[b] keys are read.  An id outside [0, num_pages)
+ *                reads as zero keys and values (no fault).
+ *   seq_lens     [B] int32, 4-byte aligned: keys of sequence b.  Values are
+ *                clamped to [0, max_seq_len]; a length of 0 gives O = 0 and
+ *                lse = -inf for that sequence.
+ *   o [B, H, d] bf16, lse [B, H] fp32 (written), as for fa_decode_splitkv.
+ *   page_size    a positive multiple of 64.  max_pages, num_pages >= 1.
+ *   max_seq_len  the longest seq_lens value, 1 .. max_pages*page_size: the
+ *                host plans the splits for it (the lengths are device data).
+ *   splits       partials per (b, h), 0 = chosen from max_seq_len and the SM
+ *                count, as for fa_decode_splitkv; a split covers at most
+ *                1023 pages (FA_ERR_UNSUPPORTED beyond).
+ *   workspace    >= fa_decode_paged_workspace_bytes(...) bytes, 256-byte aligned.
+ * Keys at or past seq_lens[b] are masked and their rows never read into O,
+ * whatever the page holds there.  Returns FA_OK once both kernels are queued.
+ */
+size_t fa_decode_paged_workspace_bytes(int B, int H, int max_seq_len, int d, int page_size, int max_pages,
+                                       int splits);
+fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int* block_table, const int* seq_lens, void* o, float* lse,
+                            int B, int H, int d, int page_size, int max_pages, int num_pages,
+                            int max_seq_len, float scale, int splits, void* workspace,
+                            size_t ws_bytes, void* stream);
+
+/*
  * fa_combine -- merge S partial (U, m, l) triples per row into O and lse:
  *     m = max_s m_s,  w_s = exp(m_s - m),  l = sum_s w_s l_s,
  *     O = sum_s w_s U_s / l,  lse = m + ln(l)

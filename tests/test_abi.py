@@ -118,3 +118,34 @@ def test_fp8_argument_checks_need_no_gpu(lib):
     assert q(vp(16), vp(24), vp(16), 1, 1, 128, 128, vp(0)) == fattn.FA_ERR_INVALID_ARG  # codes misaligned
     assert q(vp(16), vp(16), vp(0), 1, 1, 128, 128, vp(0)) == fattn.FA_ERR_INVALID_ARG
     assert q(vp(16), vp(16), vp(16), 1, 0, 128, 128, vp(0)) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_paged_decode_argument_checks_need_no_gpu(lib):
+    from exact_attention_06_gb300 import fattn
+    vp, f, sz = ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+
+    def paged(ptrs=(16,) * 7, B=2, H=4, d=128, page_size=128, max_pages=8, num_pages=16, max_seq_len=1000,
+              scale=0.1, splits=1, ws=256, ws_bytes=1 << 20):
+        return lib.fa_decode_paged(*(vp(p) for p in ptrs), B, H, d, page_size, max_pages, num_pages, max_seq_len,
+                                   f(scale), splits, vp(ws), sz(ws_bytes), vp(0))
+
+    assert paged(page_size=96) == fattn.FA_ERR_UNSUPPORTED      # not a multiple of 64
+    assert paged(page_size=0) == fattn.FA_ERR_UNSUPPORTED
+    assert paged(d=80) == fattn.FA_ERR_UNSUPPORTED
+    assert paged(max_seq_len=8 * 128 + 1) == fattn.FA_ERR_INVALID_ARG  # more than max_pages * page_size
+    assert paged(max_seq_len=0) == fattn.FA_ERR_INVALID_ARG
+    assert paged(num_pages=0) == fattn.FA_ERR_INVALID_ARG
+    assert paged(ptrs=(16, 16, 16, 0, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # null block table
+    assert paged(ptrs=(16, 16, 16, 18, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # misaligned block table
+    assert paged(ptrs=(16, 24, 16, 16, 16, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # misaligned k pool
+    assert paged(splits=-1) == fattn.FA_ERR_INVALID_ARG
+    assert paged(splits=9) == fattn.FA_ERR_INVALID_ARG            # more splits than 128-key chunks
+    assert paged(ws_bytes=16) == fattn.FA_ERR_WORKSPACE
+    # explicit splits: the workspace size needs no device and matches the contiguous decode's
+    assert fattn.fa_decode_paged_workspace_bytes(2, 4, 1000, 128, 128, 8, 2) == \
+        fattn.fa_decode_workspace_bytes(2, 4, 1000, 128, 128, 2)
+    assert fattn.fa_decode_paged_workspace_bytes(2, 4, 1000, 128, 100, 8, 2) == 0
+    # a split may cover at most 1023 pages: one split over 70000 keys of 64-key pages is refused
+    assert fattn.fa_decode_paged_workspace_bytes(1, 1, 70000, 64, 64, 1100, 1) == 0
+    assert paged(page_size=64, max_pages=1100, max_seq_len=70000, splits=1, ws_bytes=1 << 30) == \
+        fattn.FA_ERR_UNSUPPORTED

@@ -25,4 +25,5 @@ from .attention import (  # noqa: F401
     online_merge_scores,
     quantize_e4m3_blocks,
     round_to_e4m3,
+    shard_partials_head,
 )

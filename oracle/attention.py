@@ -24,6 +24,9 @@ What it computes, and where the pages define it
   equation for U_i^new; operatorworld "在线 softmax：边算边修正" update
   equations; triton-tutorial §8.3.3).  Used to pin the worked example and the
   block-split invariance; the GPU path is compared against ``attention``.
+* ``shard_partials_head`` -- one key shard's partial (U, m, l) per query row
+  (Ring Attention's local step, cnblogs §三 场景 A), the plain definition
+  restricted to the shard's admissible keys.
 * ``combine`` -- merging partial (U, m, l) triples: m = max_w m_w,
   l = sum_w exp(m_w - m) l_w, O = sum_w exp(m_w - m) U_w / l (iceferryling
   "FlashAttention 1 和 FlashAttention 2 的区别", §6 cross-warp merge; the same
@@ -241,6 +244,32 @@ def compositions(n: int):
                 run += 1
         sizes.append(run)
         yield sizes
+
+
+def shard_partials_head(q, k_shard, v_shard, scale: float, causal: bool, key_offset: int, rows=None):
+    """One query block against one key shard (Ring Attention's local step, cnblogs §三 场景 A):
+    per row the plain definition restricted to the shard's admissible keys (global index
+    key_offset + j, causal keeps those <= the row) -> (U [R, dv], m [R], l [R]) with
+    m = max s, l = sum exp(s - m), U = sum exp(s - m) v; (0, -inf, 0) for a row without keys."""
+    q, k, v = _f64(q), _f64(k_shard), _f64(v_shard)
+    n = q.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    u = np.zeros((rows.shape[0], v.shape[1]))
+    m = np.full(rows.shape[0], NEG_INF)
+    l = np.zeros(rows.shape[0])
+    s_all = float(scale) * (q[rows] @ k.T)
+    for r, i in enumerate(rows):
+        keys = np.arange(k.shape[0])
+        if causal:
+            keys = keys[key_offset + keys <= i]
+        if keys.shape[0] == 0:
+            continue
+        s = s_all[r, keys]
+        m[r] = s.max()
+        e = np.exp(s - m[r])
+        l[r] = e.sum()
+        u[r] = e @ v[keys]
+    return u, m, l
 
 
 def combine(u_parts, m_parts, l_parts):

@@ -350,3 +350,41 @@ def test_decode_is_one_row_attention():
         w = np.exp(s - s.max())
         np.testing.assert_allclose(o[idx], (w @ v[bb, hh]) / w.sum(), rtol=1e-13)
         assert lse[idx] == pytest.approx(s.max() + math.log(w.sum()), rel=1e-14)
+
+
+# ------------------------------------------------------------------ key-shard partials (Ring Attention merge)
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_shard_partials_merge_to_the_full_definition(causal):
+    # cutting the keys into shards anywhere and merging the partials with ``combine`` gives the
+    # unsharded result (cnblogs §三 场景 A; checked against torch's fp64 SDPA)
+    rng = np.random.default_rng(31)
+    n, d = 45, 6
+    q, k, v = (rng.standard_normal((n, d)) for _ in range(3))
+    cuts = [0, 7, 8, 30, 45]
+    parts = [oracle.shard_partials_head(q, k[a:b], v[a:b], 0.4, causal, a) for a, b in zip(cuts, cuts[1:])]
+    u = np.stack([p[0] for p in parts], axis=1)
+    m = np.stack([p[1] for p in parts], axis=1)
+    l = np.stack([p[2] for p in parts], axis=1)
+    o, lse = oracle.combine(u, m, l)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q)[None], torch.from_numpy(k)[None],
+                                                           torch.from_numpy(v)[None], is_causal=causal,
+                                                           scale=0.4)[0].numpy()
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-13)
+    ro, rl = oracle.attention_head(q, k, v, 0.4, causal)
+    np.testing.assert_allclose(lse, rl, rtol=0, atol=1e-13)
+    if causal:
+        # rows before a shard's first key get the empty partial (0, -inf, 0)
+        u2, m2, l2 = parts[3]  # keys 30..44
+        assert np.all(np.isneginf(m2[:30])) and np.all(l2[:30] == 0) and np.all(u2[:30] == 0)
+        assert np.all(np.isfinite(m2[30:]))
+
+
+def test_shard_partial_of_one_key_is_closed_form():
+    # a shard holding the single key j: m = scale q.k_j, l = 1, U = v_j
+    rng = np.random.default_rng(32)
+    q, k, v = (rng.standard_normal((4, 3)) for _ in range(3))
+    u, m, l = oracle.shard_partials_head(q, k[2:3], v[2:3], 0.5, False, 2)
+    np.testing.assert_allclose(m, 0.5 * q @ k[2], rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(l, 1.0)
+    np.testing.assert_array_equal(u, np.broadcast_to(v[2], (4, 3)))

@@ -237,6 +237,36 @@ def _paged_decode_step_fn(w, dev, stream, page_size=128):
     return step, 2
 
 
+def _sharded_step_fn(w, dev, stream, shards=4):
+    """Sequence-sharded prefill: the keys cut into equal shards, each in its own K/V buffers,
+    one fa_fwd_partial per shard, then fa_combine."""
+    import torch
+    from exact_attention_06_gb300 import fattn, inputs
+    q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
+    cuts = [w.N * i // shards for i in range(shards + 1)]
+    ks = [k[:, :, a:b].contiguous() for a, b in zip(cuts, cuts[1:])]
+    vs = [v[:, :, a:b].contiguous() for a, b in zip(cuts, cuts[1:])]
+    del k, v
+    R = w.B * w.H * w.N
+    u = torch.empty((R, shards, w.d), dtype=torch.float32, device=dev)
+    m = torch.empty((R, shards), dtype=torch.float32, device=dev)
+    l = torch.empty((R, shards), dtype=torch.float32, device=dev)
+    o = torch.empty((R, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(R, dtype=torch.float32, device=dev)
+
+    side = [torch.cuda.Stream(device=dev) for _ in range(shards)]
+
+    def step():
+        # the shards are independent: each on its own stream, joined before the combine
+        for s in range(shards):
+            side[s].wait_stream(stream)
+            fattn.fa_fwd_partial(q, ks[s], vs[s], u, m, l, w.scale, cuts[s], s, w.causal, stream=side[s])
+        for s in range(shards):
+            stream.wait_stream(side[s])
+        fattn.fa_combine(u, m, l, o, lse, stream=stream)
+    return step, shards + 1
+
+
 def _fp8_step_fn(w, dev, stream):
     """One FP8 forward (fa_fwd_fp8) over the workload; Q, K, V quantized to E4M3 once beforehand
     (the FP8 path keeps its inputs in HBM as codes plus block scales)."""
@@ -428,6 +458,20 @@ def run_ours(args):
             "note": "fa_decode_paged: split kernel through the block table, then the combine kernel"}
         del pst
         torch.cuda.empty_cache()
+        # sequence-sharded prefill of the causal workload: four key shards, then the combine
+        sst, nl = _sharded_step_fn(wb, dev, stream)
+        sms_ = _time_steps(sst, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
+        stt = statistics.mean(sms_)
+        extra["causal_sharded4"] = {
+            "value": round(wb.flops() / (stt * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(stt, 4), "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
+            "config": {"B": wb.B, "H": wb.H, "N": wb.N, "d": wb.d, "causal": True, "shards": 4,
+                       "spike_every_64th_key_x8": True},
+            "roofline": _roofline("tensor", wb.flops(), stt, peaks, None),
+            "note": "4 x fa_fwd_partial (one per 2048-key shard, concurrent streams) + fa_combine; "
+                    "flops of the unsharded forward"}
+        del sst
+        torch.cuda.empty_cache()
         # FP8 forward on the causal workload (E4M3 inputs with per-128-row block scales)
         fst, nl = _fp8_step_fn(wb, dev, stream)
         fms = _time_steps(fst, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
@@ -484,7 +528,8 @@ def run_ours(args):
 def run_only(args, w, dev, stream, peaks, flush):
     """One workload alone (profiler captures and sweeps): its step timed like the headline."""
     fn = (_paged_decode_step_fn if args.paged else _decode_step_fn) if w.kind == "decode" else (
-        _backward_step_fn if args.backward else (_fp8_step_fn if args.fp8 else _prefill_step_fn))
+        (lambda w_, d_, s_: _sharded_step_fn(w_, d_, s_, args.shards)) if args.shards else (
+        _backward_step_fn if args.backward else (_fp8_step_fn if args.fp8 else _prefill_step_fn)))
     step, launches = fn(w, dev, stream)
     small = w.kind == "prefill" and 3 * w.B * w.H * w.N * w.d * 2 < L2_FLUSH_BYTES
     ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush if small else None)
@@ -499,6 +544,7 @@ def run_only(args, w, dev, stream, peaks, flush):
         unit = "TFLOP/s"
         value = work / (t * 1e-3) / 1e12
     tag = (" backward" if args.backward else "") + (" fp8" if args.fp8 else "") + (" paged" if args.paged else "")
+    tag += f" sharded{args.shards}" if args.shards else ""
     print(json.dumps({"workload": w.name + tag, "value": round(value, 3), "unit": unit, "steps": args.steps,
                       "warmup": args.warmup, "ms_per_step": round(t, 5), "ms_min": round(min(ms), 5),
                       "gpu_launches": launches * args.steps,
@@ -607,6 +653,7 @@ def main():
     ap.add_argument("--backward", action="store_true", help="with --only: time fa_bwd instead of the forward")
     ap.add_argument("--fp8", action="store_true", help="with --only: time the FP8 forward (fa_fwd_fp8)")
     ap.add_argument("--paged", action="store_true", help="with --only and a decode workload: time fa_decode_paged")
+    ap.add_argument("--shards", type=int, default=0, help="with --only and a prefill workload: key shards + combine")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

@@ -309,26 +309,61 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
 }
 
+// One warp per row, kCombineRows rows per CTA: lane l holds columns [l*D/32, (l+1)*D/32).
+// The row's partial maxima are read 32 at a time (one per lane) and reduced by shuffles; then
+// each partial's U slice is one vector load per lane.  Empty partials (m = -inf) are skipped
+// without reading their U or l.
+constexpr int kCombineRows = 8;
+
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(32 * kCombineRows)
     combine_kernel(const float* __restrict__ u_part, const float* __restrict__ m_part,
-                   const float* __restrict__ l_part, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int S) {
-  const size_t r = blockIdx.x;
-  const int t = threadIdx.x;
+                   const float* __restrict__ l_part, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int R,
+                   int S) {
+  constexpr int C = D / 32;  // columns per lane: 2 or 4
+  const int lane = threadIdx.x & 31;
+  const long long r = static_cast<long long>(blockIdx.x) * kCombineRows + (threadIdx.x >> 5);
+  if (r >= R) return;
   const float* mr = m_part + r * S;
   const float* lr = l_part + r * S;
-  const float* ur = u_part + r * S * D;
+  const float* ur = u_part + r * S * D + lane * C;
   float mm = -INFINITY;
-  for (int s = 0; s < S; ++s) mm = fmaxf(mm, mr[s]);
-  const float mb = (mm == -INFINITY) ? 0.f : mm;
-  float lt = 0.f, acc = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float w = expf(mr[s] - mb);  // empty partial: exp(-inf) = 0
-    lt = fmaf(w, lr[s], lt);
-    acc = fmaf(w, ur[static_cast<size_t>(s) * D + t], acc);
+  for (int s = lane; s < S; s += 32) mm = fmaxf(mm, mr[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+  float lt = 0.f, acc[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) acc[i] = 0.f;
+  if (mm != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float ms = mr[s];
+      if (ms == -INFINITY) continue;  // empty partial: weight 0, U and l not read
+      const float w = expf(ms - mm);
+      lt = fmaf(w, lr[s], lt);
+      if constexpr (C == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(ur + static_cast<size_t>(s) * D);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+        acc[2] = fmaf(w, x.z, acc[2]);
+        acc[3] = fmaf(w, x.w, acc[3]);
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(ur + static_cast<size_t>(s) * D);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+      }
+    }
   }
-  o[r * D + t] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
-  if (t == 0) lse[r] = lt > 0.f ? mm + logf(lt) : -INFINITY;
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
+  __nv_bfloat16* orow = o + r * D + lane * C;
+  if constexpr (C == 4) {
+    uint2 w2;
+    w2.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    w2.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(orow) = w2;
+  } else {
+    *reinterpret_cast<uint32_t*>(orow) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0) lse[r] = lt > 0.f ? mm + logf(lt) : -INFINITY;
 }
 
 template <int D, bool PAGED>
@@ -354,12 +389,13 @@ cudaError_t launch_decode_split(const DecodeLaunch& a, cudaStream_t stream) {
 
 cudaError_t launch_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
                            int S, int d, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((R + kCombineRows - 1) / kCombineRows);
   if (d == 64)
-    combine_kernel<64><<<static_cast<unsigned>(R), 64, 0, stream>>>(u_part, m_part, l_part,
-                                                                     static_cast<__nv_bfloat16*>(o), lse, S);
+    combine_kernel<64><<<grid, 32 * kCombineRows, 0, stream>>>(u_part, m_part, l_part,
+                                                               static_cast<__nv_bfloat16*>(o), lse, R, S);
   else
-    combine_kernel<128><<<static_cast<unsigned>(R), 128, 0, stream>>>(u_part, m_part, l_part,
-                                                                       static_cast<__nv_bfloat16*>(o), lse, S);
+    combine_kernel<128><<<grid, 32 * kCombineRows, 0, stream>>>(u_part, m_part, l_part,
+                                                                static_cast<__nv_bfloat16*>(o), lse, R, S);
   return cudaGetLastError();
 }
 

@@ -158,13 +158,42 @@ __device__ __forceinline__ void store_half_row(void* o, float* lse, size_t row_o
   if (h == 0) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
 }
 
+// This thread's half of a partial (U, m, l) row for a key shard: U unnormalised (relative to
+// exp(s - m)), m in natural-log units, l; an empty row (no admissible key) gets m = -inf,
+// l = 0 and no U.
+template <int D>
+__device__ __forceinline__ void store_half_partial(const FwdAux& aux, size_t prow, int h, bool valid, uint32_t taddr,
+                                                   float l, float m2, bool have_u) {
+  uint32_t ur[D / 2];
+  if (have_u) {
+    if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
+  }
+  if (!valid) return;
+  const size_t slot = prow * aux.S + aux.shard;
+  const bool empty = !(l > 0.f);
+  if (!empty) {  // an empty partial's U is never read (the combine skips m = -inf)
+    float4* dst = reinterpret_cast<float4*>(aux.u_part + slot * D + h * (D / 2));
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      dst[i] = make_float4(__uint_as_float(ur[4 * i]), __uint_as_float(ur[4 * i + 1]),
+                           __uint_as_float(ur[4 * i + 2]), __uint_as_float(ur[4 * i + 3]));
+  }
+  if (h == 0) {
+    aux.m_part[slot] = empty ? -INFINITY : m2 * kLn2;
+    aux.l_part[slot] = empty ? 0.f : l;
+  }
+}
+
 template <int D, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, void* __restrict__ o, float* __restrict__ lse, int N,
-               float sl2, int o_fp32, unsigned long long budget, const float* __restrict__ sq,
-               const float* __restrict__ sk, const float* __restrict__ sv) {
+               float sl2, int o_fp32, unsigned long long budget, const FwdAux aux) {
   using C = FwdCfg<D, FP8>;
+  const float* __restrict__ sq = aux.sq;
+  const float* __restrict__ sk = aux.sk;
+  const float* __restrict__ sv = aux.sv;
+  const int Nk = aux.Nk, koff = aux.koff;  // this launch's keys: global indices koff .. koff + Nk - 1
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -179,11 +208,15 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest causal work first
-  const int n_tiles = (N + kBc - 1) / kBc;
-  // KV steps of each query tile: all key tiles, or (causal) those up to its diagonal; 0 if the tile is past N.
+  const int n_tiles = (Nk + kBc - 1) / kBc;
+  // KV steps of each query tile: all key tiles, or (causal) those holding a key at or before
+  // its last row; 0 if the tile is past N.
   auto steps_of = [&](int t) {
     const int row0 = pair * kRowsPerCta + t * kBr;
-    return row0 >= N ? 0 : (CAUSAL ? min(row0 / kBc + 1, n_tiles) : n_tiles);
+    if (row0 >= N) return 0;
+    if (!CAUSAL) return n_tiles;
+    const int keys = min(row0 + kBr, N) - koff;  // admissible keys of the tile's last row
+    return keys <= 0 ? 0 : min((keys + kBc - 1) / kBc, n_tiles);
   };
   const int n_t0 = steps_of(0), n_t1 = steps_of(1);
   const int n_max = max(n_t0, n_t1);
@@ -391,7 +424,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           mma_o(j > 0 || kk > 0, d_o, a_p + static_cast<uint32_t>(kk) * 8u,
                 sdesc_add(dv, static_cast<uint32_t>(kk * C::K_MMA) * 128u));
       };
-      bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, budget, &g_fwd_status) &&
+      // n_max = 0 (a key shard after both tiles' rows): no K/V is loaded and nothing is issued
+      bool ok = n_max > 0 && mbar_wait(BAR(C::B_Q), 0, abort_flag, budget, &g_fwd_status) &&
                 mbar_wait(BAR(C::B_KF), 0, abort_flag, budget, &g_fwd_status);
       if (ok) {
         tc_fence_after();
@@ -459,8 +493,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     const uint32_t t_s = tmem + lane_addr + static_cast<uint32_t>(t * kBc);
     const uint32_t t_o = tmem + lane_addr + kColO + static_cast<uint32_t>(t * D);
     const uint32_t t_p = tmem + lane_addr + C::COL_P + 64u * t;  // separate P~ columns (d = 64)
-    const int lim = CAUSAL ? min(row, N - 1) : N - 1;  // last admissible key of this row
-    const int n_kt = (N + kBc - 1) / kBc;
+    const int lim = CAUSAL ? min(row - koff, Nk - 1) : Nk - 1;  // last admissible key of this row (local index)
+    const int n_kt = (N + kBc - 1) / kBc;  // FP8 scale blocks per head (FP8 launches have Nk = N, koff = 0)
     // Q block scale (read only for a tile inside N: the scale array has ceil(N/128) entries per head)
     const float sq_t = (FP8 && n > 0) ? sq[static_cast<size_t>(bh) * n_kt + pair * 2 + t] : 1.f;
     const float sv_max = FP8 ? *sv_max_slot : 1.f;
@@ -583,8 +617,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
-      store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
-                        FP8 ? sv_max * (1.f / 256.f) : 1.f);
+      if (aux.u_part)
+        store_half_partial<D>(aux, static_cast<size_t>(bh) * N + row, h, row < N, t_o, l_row, m2, true);
+      else
+        store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
+                          FP8 ? sv_max * (1.f / 256.f) : 1.f);
+    } else if (aux.u_part && n == 0) {
+      // no key of this shard is admissible for the tile: an empty partial, U never touched
+      store_half_partial<D>(aux, static_cast<size_t>(bh) * N + row, h, row < N, t_o, 0.f, -INFINITY, false);
     }
     tmem_wait_st();
   }
@@ -606,7 +646,7 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
   const int n_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget,
-                                              a.sq, a.sk, a.sv);
+                                              a.aux);
   return cudaGetLastError();
 }
 

@@ -237,6 +237,7 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   a.o_fp32 = o_fp32;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
+  a.aux.Nk = N;
   cudaGetLastError();  // clear a stale, non-sticky error so that it is not blamed on this launch
   cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
@@ -246,6 +247,49 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                    float scale, int causal, void* stream) {
   return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, stream, nullptr);
+}
+
+fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u_part, float* m_part,
+                           float* l_part, int B, int H, int N, int Nk, int key_offset, int d, float scale, int causal,
+                           int shard, int S, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !u_part || !m_part || !l_part) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (B < 1 || H < 1 || N < 1 || Nk < 1)
+    return fail(FA_ERR_INVALID_ARG, "B, H, N and Nk must be >= 1 (got %d, %d, %d, %d)", B, H, N, Nk);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (key_offset < 0) return fail(FA_ERR_INVALID_ARG, "key_offset=%d must be >= 0", key_offset);
+  if (S < 1 || shard < 0 || shard >= S) return fail(FA_ERR_INVALID_ARG, "shard=%d must be in [0, S=%d)", shard, S);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(u_part, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v and u_part must be 16-byte aligned");
+  if (!aligned(m_part, 4) || !aligned(l_part, 4)) return fail(FA_ERR_INVALID_ARG, "m_part, l_part must be 4-byte aligned");
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
+  if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 query-tile grid limit", N);
+  fa_status_t st = check_device(nullptr);
+  if (st != FA_OK) return st;
+  fattn::FwdLaunch a{};
+  if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tk, k, d, Nk, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v, d, Nk, bh, 128)) != FA_OK) return st;
+  a.N = N;
+  a.BH = static_cast<int>(bh);
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.budget = kDefaultBudget;
+  a.aux.Nk = Nk;
+  a.aux.koff = key_offset;
+  a.aux.u_part = u_part;
+  a.aux.m_part = m_part;
+  a.aux.l_part = l_part;
+  a.aux.shard = shard;
+  a.aux.S = S;
+  cudaGetLastError();
+  cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_partial launch");
+  return FA_OK;
 }
 
 fa_status_t fa_quantize_e4m3(const void* x, void* codes, float* scales, int B, int H, int N, int d, void* stream) {
@@ -300,9 +344,10 @@ fa_status_t fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const flo
   a.scale_log2 = scale * 1.4426950408889634f;
   a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
   a.fp8 = 1;
-  a.sq = sq;
-  a.sk = sk;
-  a.sv = sv;
+  a.aux.sq = sq;
+  a.aux.sk = sk;
+  a.aux.sv = sv;
+  a.aux.Nk = N;
   cudaGetLastError();
   cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");

@@ -18,6 +18,19 @@ constexpr unsigned long long kDrainBudget = kDefaultBudget;
 // Forward (prefill) launch description.  The tensor maps describe q, k, v as
 // 3-D tensors {d, N, B*H} (innermost first) with 64 x 128 boxes and 128-byte
 // swizzle.
+// Per-launch extras of the forward kernel, passed by value.
+struct FwdAux {
+  const float* sq;  // FP8: block scales [BH, ceil(N/128)] of q, k, v
+  const float* sk;
+  const float* sv;
+  int Nk;           // keys of this launch (= N unless a key shard)
+  int koff;         // global index of key 0 (causal masking of a key shard)
+  float* u_part;    // key shard: partials [BH*N, S, d], [BH*N, S], [BH*N, S]; null = write O, lse
+  float* m_part;
+  float* l_part;
+  int shard, S;
+};
+
 struct FwdLaunch {
   CUtensorMap tq, tk, tv;
   void* o;
@@ -29,10 +42,8 @@ struct FwdLaunch {
   int o_fp32;
   float scale_log2;  // scale * log2(e)
   unsigned long long budget;
-  int fp8;            // 1: q, k, v are E4M3 with per-128-row block scales sq, sk, sv (d = 128)
-  const float* sq;
-  const float* sk;
-  const float* sv;
+  int fp8;            // 1: q, k, v are E4M3 with per-128-row block scales in aux (d = 128)
+  FwdAux aux;
 };
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 unsigned int fwd_read_and_clear_status();

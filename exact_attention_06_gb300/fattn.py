@@ -25,7 +25,7 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
             "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes", "fa_decode_paged",
             "fa_combine", "fa_get_status", "fa_status_string",
             "fa_last_error")
@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
+        L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp]
         L.fa_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, i, vp]
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
@@ -73,7 +74,7 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd", "fa_decode_splitkv",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd", "fa_decode_splitkv",
                      "fa_decode_splitkv_noalloc", "fa_decode_paged",
                      "fa_combine", "fa_get_status"):
             getattr(L, name).restype = i
@@ -129,6 +130,18 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None):
     st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
                       _stream(stream))
     _check(st, "fa_fwd")
+
+
+def fa_fwd_partial(q, k, v, u_part, m_part, l_part, scale: float, key_offset: int, shard: int,
+                   causal: bool = False, stream=None):
+    """Forward over one key shard: q [B, H, N, d]; k, v [B, H, Nk, d] (global key indices from
+    key_offset); writes slot ``shard`` of u_part [B*H*N, S, d], m_part / l_part [B*H*N, S] fp32."""
+    B, H, N, d = q.shape
+    Nk = k.shape[2]
+    S = u_part.shape[1]
+    st = lib().fa_fwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(u_part), _ptr(m_part), _ptr(l_part), B, H, N, Nk,
+                              int(key_offset), d, float(scale), int(bool(causal)), int(shard), S, _stream(stream))
+    _check(st, "fa_fwd_partial")
 
 
 def fa_quantize_e4m3(x, codes, scales, stream=None):

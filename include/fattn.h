@@ -84,6 +84,33 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
                       const fa_fwd_opts* opts);
 
 /*
+ * fa_fwd_partial -- the forward over one shard of the keys, leaving a partial
+ * (U, m, l) per query row for fa_combine instead of O and lse.  This is the
+ * sequence-sharded prefill of Ring Attention without the ring: each KV shard
+ * is one pass of the forward kernel, and the partials merge by the
+ * online-softmax rule (cnblogs jzssuanfa page, §三 场景 A; xuesongtap §5).
+ *
+ *   q        [B, H, N, d] bf16, 16-byte aligned: every query row.
+ *   k, v     [B, H, Nk, d] bf16, 16-byte aligned: the shard's keys, whose
+ *            global indices are key_offset .. key_offset + Nk - 1.
+ *   u_part   [B*H*N, S, d] fp32, 16-byte aligned: slot `shard` of each row is
+ *            written with U = sum_j exp(s_j - m) v_j over the row's admissible
+ *            keys of the shard.
+ *   m_part,  [B*H*N, S] fp32, 4-byte aligned: slot `shard` gets m (the row max
+ *   l_part   of the scaled scores, natural-log units) and l = sum_j exp(s_j - m).
+ *            A row with no admissible key in the shard gets m = -inf and
+ *            l = 0; its U slot is left as it was (fa_combine does not read it).
+ *   causal   1: query i attends global keys j <= i (top-left aligned).
+ *   d in {64, 128}; 0 <= shard < S; key_offset >= 0; other arguments as fa_fwd.
+ * After one call per shard (any order, any stream order that completes them
+ * first), fa_combine(u_part, m_part, l_part, o, lse, B*H*N, S, d) gives the
+ * forward over all the shards' keys.
+ */
+fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u_part, float* m_part,
+                           float* l_part, int B, int H, int N, int Nk, int key_offset, int d,
+                           float scale, int causal, int shard, int S, void* stream);
+
+/*
  * fa_quantize_e4m3 -- block quantization of Q, K or V for fa_fwd_fp8
  * (triton-tutorial "8. FlashAttention 实战", §8.9.4: one scale per block of
  * 128 rows x d; scale = max|x| / 448, 448 being E4M3's largest finite value).
@@ -241,8 +268,8 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
  *   u_part [R, S, d] fp32, unnormalised numerators (relative to exp(s - m_s)).
  *   m_part [R, S] fp32, row maxima in natural-log units of scaled scores.
  *   l_part [R, S] fp32, denominators.
- *   An empty partial (m = -inf, l = 0) has weight 0; a row whose partials are
- *   all empty gets O = 0 and lse = -inf.
+ *   An empty partial (m = -inf) has weight 0 and its U and l are not read;
+ *   a row whose partials are all empty gets O = 0 and lse = -inf.
  *   o [R, d] bf16 (written), lse [R] fp32 (written).  R, S >= 1, d in {64, 128}.
  *   u_part 16-byte aligned; m_part, l_part, lse 4-byte aligned; o 16-byte aligned.
  */

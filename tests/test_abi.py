@@ -149,3 +149,20 @@ def test_paged_decode_argument_checks_need_no_gpu(lib):
     assert fattn.fa_decode_paged_workspace_bytes(1, 1, 70000, 64, 64, 1100, 1) == 0
     assert paged(page_size=64, max_pages=1100, max_seq_len=70000, splits=1, ws_bytes=1 << 30) == \
         fattn.FA_ERR_UNSUPPORTED
+
+
+def test_partial_forward_argument_checks_need_no_gpu(lib):
+    from exact_attention_06_gb300 import fattn
+    vp, f = ctypes.c_void_p, ctypes.c_float
+
+    def part(ptrs=(16,) * 6, N=256, Nk=128, koff=0, d=128, shard=0, S=2, causal=1):
+        return lib.fa_fwd_partial(*(vp(p) for p in ptrs), 1, 2, N, Nk, koff, d, f(0.1), causal, shard, S, vp(0))
+
+    assert part(shard=2) == fattn.FA_ERR_INVALID_ARG
+    assert part(shard=-1) == fattn.FA_ERR_INVALID_ARG
+    assert part(S=0) == fattn.FA_ERR_INVALID_ARG
+    assert part(koff=-5) == fattn.FA_ERR_INVALID_ARG
+    assert part(Nk=0) == fattn.FA_ERR_INVALID_ARG
+    assert part(d=96) == fattn.FA_ERR_UNSUPPORTED
+    assert part(ptrs=(16, 16, 16, 8, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # u_part misaligned
+    assert part(ptrs=(16, 16, 16, 16, 0, 16)) == fattn.FA_ERR_INVALID_ARG

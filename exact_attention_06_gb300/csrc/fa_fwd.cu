@@ -439,7 +439,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       }
       static_assert(!C::SEP, "the separate-P~ schedule runs with an MMA warp per tile");
       for (int j = 1; ok && j <= n_max; ++j) {
-        bool v_ready = false, k_ready = false;
+        // This iteration's operands first (V_{j-1} for the PVs, K_j for the next S; both are
+        // normally loaded long before), so that once a tile's P~ is ready its 2x(ROW/32) MMAs
+        // issue back to back: a wait between them lets the tensor pipe drain.
+        ok = mbar_wait(BAR(C::B_VF + (j - 1) % C::VST), ((j - 1) / C::VST) & 1, abort_flag, budget,
+                       &g_fwd_status) &&
+             (j >= n_max ||
+              mbar_wait(BAR(C::B_KF + j % C::KST), (j / C::KST) & 1, abort_flag, budget, &g_fwd_status));
+        if (!ok) break;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int nt = t ? n_t1 : n_t0;
@@ -448,28 +455,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
             ok = false;
             break;
           }
-          if (!v_ready) {
-            const int vs = (j - 1) % C::VST;
-            if (!mbar_wait(BAR(C::B_VF + vs), ((j - 1) / C::VST) & 1, abort_flag, budget, &g_fwd_status)) {
-              ok = false;
-              break;
-            }
-            v_ready = true;
-          }
           tc_fence_after();
           issue_pv(t, j - 1);
-          if (j < nt) {
-            if (!k_ready) {
-              const int ks = j % C::KST;
-              if (!mbar_wait(BAR(C::B_KF + ks), (j / C::KST) & 1, abort_flag, budget, &g_fwd_status)) {
-                ok = false;
-                break;
-              }
-              k_ready = true;
-              tc_fence_after();
-            }
-            issue_s(t, j);
-          }
+          if (j < nt) issue_s(t, j);
           tc_commit(BAR(C::B_SF + t));  // S_t(j) ready, and PV_t(j-1) done: U_t may be rescaled
         }
         if (!ok) break;
@@ -500,12 +488,21 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     const float sv_max = FP8 ? *sv_max_slot : 1.f;
     float m2 = -INFINITY, l = 0.f;  // l: this thread's half of the row
     bool ok = n > 0;
+    // FP8: key tile j's K and V block scales, loaded one step ahead
+    const float* sk_h = FP8 ? sk + static_cast<size_t>(bh) * n_kt : nullptr;
+    const float* sv_h = FP8 ? sv + static_cast<size_t>(bh) * n_kt : nullptr;
+    float sk_next = (FP8 && n > 0) ? sk_h[0] : 1.f, sv_next = (FP8 && n > 0) ? sv_h[0] : 1.f;
     for (int j = 0; ok && j < n; ++j) {
+      const float sk_j = sk_next, sv_j = sv_next;
+      if (FP8 && j + 1 < n) {
+        sk_next = sk_h[j + 1];
+        sv_next = sv_h[j + 1];
+      }
       ok = wait_all(BAR(C::B_SF + t), j & 1, abort_flag, budget);
       if (!ok) break;
       tc_fence_after();
       // exponent multiplier of this key tile: scale * log2(e), times the dequantization scales (FP8)
-      const float cj = FP8 ? sq_t * sk[static_cast<size_t>(bh) * n_kt + j] * sl2 : sl2;
+      const float cj = FP8 ? sq_t * sk_j * sl2 : sl2;
       const uint64_t c2 = f2_pack(cj, cj);
       uint32_t sr[64];
       tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
@@ -563,21 +560,26 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         for (int i = 0; i < 32; ++i) pr[i] = sr[i];
         tmem_st2_x32<32>(t_p, pr);
       }
+      float inv_ps = 1.f;  // FP8: the row sum below is of p * ps; l takes p
       if constexpr (FP8) {
-        // P~ as E4M3 of p * 256 * sv_j / sv_max (<= 256): the V block scale rides on P~ so that
-        // U accumulates in one unit for every key tile; 4 keys per TMEM column.
-        const float ps = 256.f * sv[static_cast<size_t>(bh) * n_kt + j] / sv_max;
+        // P~ as E4M3 of p * ps, ps = 256 * sv_j / sv_max (<= 256): the V block scale rides on P~
+        // so that U accumulates in one unit for every key tile; 4 keys per TMEM column.  ps is
+        // folded into the exponent: p * ps = 2^(s c - m + log2 ps).
+        const float ps = 256.f * sv_j / sv_max;
+        inv_ps = sv_max / (256.f * sv_j);
+        const float lps = log2f(ps);
+        const uint64_t nmp2 = f2_pack(lps - mb, lps - mb);
         uint32_t pr[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2, nmb2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2, nmb2), x2,
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2, nmp2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2, nmp2), x2,
                     x3);
           const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           rs_a = f2_add(rs_a, f2_pack(p0, p1));
           rs_b = f2_add(rs_b, f2_pack(p2, p3));
-          pr[i] = pack_e4m3x4(p0 * ps, p1 * ps, p2 * ps, p3 * ps);
+          pr[i] = pack_e4m3x4(p0, p1, p2, p3);
         }
         tmem_st2_x16<16>(t_s, pr);  // keys 64h + 4i .. +3 -> column 16h + i
       }
@@ -602,7 +604,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       float s0, s1, s2, s3;
       f2_unpack(rs_a, s0, s1);
       f2_unpack(rs_b, s2, s3);
-      l = fmaf(alpha, l, (s0 + s1) + (s2 + s3));
+      l = fmaf(alpha, l, ((s0 + s1) + (s2 + s3)) * inv_ps);
       // PV_t(j-1) is complete (the commit that announced S_t(j) covers it): rescale U_t in place.
       if (!C::SEP && j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
       tmem_wait_st();

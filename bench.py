@@ -59,10 +59,17 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.392e6,
-                                "sha256": "fc30fa2f9407e04d0607c6192f48ca8c98cffd32d2410e9fa9b67da1d7f874c6"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 588.989e6,
-                               "sha256": "fc30fa2f9407e04d0607c6192f48ca8c98cffd32d2410e9fa9b67da1d7f874c6"},
+    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.447e6,
+                                "sha256": "b2f4f95f98efaf4c389795b5f65d8526a6c81ca12e0817fc538828c77851f327"},
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 587.789e6,
+                               "sha256": "b2f4f95f98efaf4c389795b5f65d8526a6c81ca12e0817fc538828c77851f327"},
+    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 199.790e6,
+                                   "sha256": "b2f4f95f98efaf4c389795b5f65d8526a6c81ca12e0817fc538828c77851f327"},
+    # decode: captured on the B4 slice (decode_small) and scaled by 16 to B64 (K/V streamed once)
+    ("decode_split_kernel", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2151.272e6,
+                                        "sha256": "f5a79caa980ce126dce15dbfcad29b01d9650f5ef0e0a34ba9b96520a131e5e1"},
+    ("decode_split_kernel_paged", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2151.041e6,
+                                              "sha256": "f5a79caa980ce126dce15dbfcad29b01d9650f5ef0e0a34ba9b96520a131e5e1"},
 }
 
 
@@ -454,7 +461,7 @@ def run_ours(args):
             "value": round(wd.kv_bytes() / (pt * 1e-3) / 1e9 * world, 3), "unit": "GB/s",
             "ms_per_step": round(pt, 4), "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
             "config": {"B": wd.B, "H": wd.H, "L": wd.N, "d": wd.d, "page_size": 128, "pool": "shuffled pages"},
-            "roofline": _roofline("hbm", wd.kv_bytes(), pt, peaks, None),
+            "roofline": _roofline("hbm", wd.kv_bytes(), pt, peaks, _traffic("decode_split_kernel_paged", "decode")),
             "note": "fa_decode_paged: split kernel through the block table, then the combine kernel"}
         del pst
         torch.cuda.empty_cache()

@@ -166,3 +166,13 @@ def test_partial_forward_argument_checks_need_no_gpu(lib):
     assert part(d=96) == fattn.FA_ERR_UNSUPPORTED
     assert part(ptrs=(16, 16, 16, 8, 16, 16)) == fattn.FA_ERR_INVALID_ARG  # u_part misaligned
     assert part(ptrs=(16, 16, 16, 16, 0, 16)) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    # no fallback: a missing libfattn.so is an error, not a silent CPU path
+    from exact_attention_06_gb300 import fattn
+    monkeypatch.setattr(fattn, "_lib", None)
+    monkeypatch.setattr(fattn, "LIB_PATH", str(tmp_path / "libfattn.so"))
+    with pytest.raises(fattn.FattnError) as ei:
+        fattn.lib()
+    assert "missing" in str(ei.value)

@@ -82,8 +82,17 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+_STATUS_NAMES = {FA_OK: "FA_OK", FA_ERR_INVALID_ARG: "FA_ERR_INVALID_ARG", FA_ERR_UNSUPPORTED: "FA_ERR_UNSUPPORTED",
+                 FA_ERR_ARCH: "FA_ERR_ARCH", FA_ERR_CUDA: "FA_ERR_CUDA", FA_ERR_TIMEOUT: "FA_ERR_TIMEOUT",
+                 FA_ERR_WORKSPACE: "FA_ERR_WORKSPACE"}
+
+
 def status_string(status: int) -> str:
-    return lib().fa_status_string(int(status)).decode()
+    """The library's name for a status; the enum's name when the library is not loaded
+    (so that the error raised for a missing library can be built)."""
+    if _lib is None:
+        return _STATUS_NAMES.get(int(status), "FA_ERR_UNKNOWN")
+    return _lib.fa_status_string(int(status)).decode()
 
 
 def fa_status_string(status: int) -> str:

@@ -93,7 +93,7 @@ struct BwdCfg {
   static constexpr int NH = D / 64;
   static constexpr uint32_t TB = NH * kBox;   // bytes of one 128 x d bf16 tile
   static constexpr int ST = (D == 128) ? 2 : 4;
-  static constexpr uint32_t VEC = 2 * kTile * 4;  // lse2[128] + D[128] fp32 per stage (dkdv only)
+  static constexpr uint32_t VEC = 2 * kTile * 4;  // per stage (dkdv only): {-lse2, -D} of 128 rows, see OFF_VEC
   static constexpr uint32_t COL_G2 = kColG1 + D;  // second gradient accumulator (dK)
 };
 
@@ -151,6 +151,54 @@ __device__ __forceinline__ void issue_grad(uint32_t d_tmem, uint32_t a_tmem, uin
     mma_ts_c<1>(d_tmem, a_tmem + packed_col(kk), sdesc_add(db, static_cast<uint32_t>(kk) * 2048u), idesc);
 }
 
+// Elementwise step of the dK/dV kernel on 32 query columns of one key row (column pairs packed
+// as f32x2): P^T = 2^(S^T c - lse2), dS^T = P^T (dP^T - D), both rounded to bf16 pairs.  MASK
+// (the diagonal tile only) zeroes P^T where the query precedes the key.
+template <bool MASK>
+__device__ __forceinline__ void ew_pairs_dkdv(const uint32_t (&sv)[32], const uint32_t (&pv)[32], const float4* nv,
+                                              uint64_t c2, int col0, int qrow0, int key, uint32_t (&pp)[16],
+                                              uint32_t (&dp)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const int col = col0 + e;  // query row within the tile
+    const float4 x = nv[col >> 1];
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, f2_pack(x.x, x.y)), x0, x1);
+    float p0 = ex2(x0), p1 = ex2(x1);
+    if (MASK) {
+      if (qrow0 + col < key) p0 = 0.f;
+      if (qrow0 + col + 1 < key) p1 = 0.f;
+    }
+    const uint64_t p2 = f2_pack(p0, p1);
+    float s0, s1;
+    f2_unpack(f2_mul(p2, f2_add(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), f2_pack(x.z, x.w))),
+              s0, s1);
+    pp[e / 2] = pack_bf16(p0, p1);
+    dp[e / 2] = pack_bf16(s0, s1);
+  }
+}
+
+// Elementwise step of the dQ kernel on 32 key columns of one query row: dS = P (dP - D) with
+// P = 2^(S c - lse2), rounded to bf16 pairs.  MASK zeroes keys past the row's last key.
+template <bool MASK>
+__device__ __forceinline__ void ew_pairs_dq(const uint32_t (&sv)[32], const uint32_t (&pv)[32], uint64_t c2,
+                                            uint64_t nl2, uint64_t nd2, int key0, int lim, uint32_t (&dp)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl2), x0, x1);
+    float p0 = ex2(x0), p1 = ex2(x1);
+    if (MASK) {
+      if (key0 + e > lim) p0 = 0.f;
+      if (key0 + e + 1 > lim) p1 = 0.f;
+    }
+    float s0, s1;
+    f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), nd2)), s0,
+              s1);
+    dp[e / 2] = pack_bf16(s0, s1);
+  }
+}
+
 // --------------------------------------------------------------------- dK, dV: one CTA per key tile
 // TMEM: S^T at 0 (P^T packed into it), dP^T at 128 (dS^T packed into it), dV at 256, dK at 256 + d.
 template <int D>
@@ -159,7 +207,8 @@ struct DkdvCfg : BwdCfg<D> {
   static constexpr uint32_t OFF_K = 0, OFF_V = B::TB;
   static constexpr uint32_t OFF_RING = 2 * B::TB;                   // stage: Q_i, dO_i
   static constexpr uint32_t STAGE = 2 * B::TB;
-  static constexpr uint32_t OFF_VEC = OFF_RING + B::ST * STAGE;     // stage: lse2[128], D[128]
+  // stage: float4 per query-row pair {-lse2[2p], -lse2[2p+1], -D[2p], -D[2p+1]}, lse2 = lse * log2(e)
+  static constexpr uint32_t OFF_VEC = OFF_RING + B::ST * STAGE;
   static constexpr uint32_t OFF_BAR = OFF_VEC + B::ST * B::VEC;
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
                        B_DRAIN = B_PF + 1, NBAR = B_DRAIN + 1;
@@ -240,14 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(st + C::TB + h * kBox, &tdo, BAR(C::B_FULL + s), h * 64, qt * kTile, bh);
         }
       }
-      // lse (as log2 units) and D of the tile's 128 query rows; rows past N get lse = +inf, so P = 0.
+      // -lse (log2 units) and -D of the tile's 128 query rows, pairs of rows in one float4 (the
+      // elementwise warps add them with packed f32x2 operations); rows past N get -lse = -inf, so P = 0.
       float* vs = vec + s * (2 * kTile);
 #pragma unroll
       for (int c = 0; c < kTile / 32; ++c) {
-        const int r = qt * kTile + 32 * c + lane;
+        const int col = 32 * c + lane;
+        const int r = qt * kTile + col;
         const bool in = r < N;
-        vs[32 * c + lane] = in ? lse[static_cast<size_t>(bh) * N + r] * kLog2e : INFINITY;
-        vs[kTile + 32 * c + lane] = in ? delta[static_cast<size_t>(bh) * N + r] : 0.f;
+        vs[4 * (col >> 1) + (col & 1)] = in ? -lse[static_cast<size_t>(bh) * N + r] * kLog2e : -INFINITY;
+        vs[4 * (col >> 1) + 2 + (col & 1)] = in ? -delta[static_cast<size_t>(bh) * N + r] : 0.f;
       }
       mbar_arrive(BAR(C::B_FULL + s));
       issued = i + 1;
@@ -298,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = kt * kTile + r;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
     const uint32_t tA = tmem + lane_addr + kColA, tB = tmem + lane_addr + kColB;
+    const uint64_t c2 = f2_pack(sl2, sl2);
     bool ok = true;
     for (int i = 0; ok && i < n_i; ++i) {
       const int s = i % C::ST;
@@ -306,8 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int qt = i0 + i;
-      const float* lse2 = vec + s * (2 * kTile);
-      const float* dd = lse2 + kTile;
+      const float4* nv = reinterpret_cast<const float4*>(vec + s * (2 * kTile));
+      // Causal: only the diagonal query tile (qt == kt) holds pairs with query < key.
+      const bool diag = CAUSAL && qt == kt;
       // this thread's 64 query columns, two chunks of 32
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -315,21 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld2_x32<64>(tA + 32 * c, sv);
         tmem_ld2_x32<64>(tB + 32 * c, pv);
         uint32_t pp[16], dp[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = 64 * h + 32 * c + e;        // query row within the tile
-          const int qrow = qt * kTile + col;
-          float p0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2[col]));
-          float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2[col + 1]));
-          if (CAUSAL) {
-            if (qrow < key) p0 = 0.f;
-            if (qrow + 1 < key) p1 = 0.f;
-          }
-          const float s0 = p0 * (__uint_as_float(pv[e]) - dd[col]);
-          const float s1 = p1 * (__uint_as_float(pv[e + 1]) - dd[col + 1]);
-          pp[e / 2] = pack_bf16(p0, p1);
-          dp[e / 2] = pack_bf16(s0, s1);
-        }
+        if (diag) ew_pairs_dkdv<true>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
+        else ew_pairs_dkdv<false>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
         tmem_st2_x16<64>(tA + 16 * c, pp);  // P^T packed: columns 64h + 16c ..
         tmem_st2_x16<64>(tB + 16 * c, dp);  // dS^T packed
       }
@@ -483,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = in ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : INFINITY;
     const float dd = in ? delta[static_cast<size_t>(bh) * N + row] : 0.f;
     const int lim = CAUSAL ? min(row, N - 1) : N - 1;  // last key this row attends
+    const uint64_t c2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-dd, -dd);
     bool ok = true;
     for (int j = 0; ok && j < n_j; ++j) {
       ok = bwait_all(BAR(C::B_SF), j & 1, abort_flag, budget);
@@ -495,14 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld2_x32<64>(tB + 32 * c, pv);
         uint32_t dp[16];
         const int key0 = j * kTile + 64 * h + 32 * c;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2));
-          if (key0 + e > lim) p0 = 0.f;
-          if (key0 + e + 1 > lim) p1 = 0.f;
-          dp[e / 2] = pack_bf16(p0 * (__uint_as_float(pv[e]) - dd), p1 * (__uint_as_float(pv[e + 1]) - dd));
-        }
+        // only the diagonal and the ragged last key tile reach past this row's last key
+        if (key0 + 31 > lim) ew_pairs_dq<true>(sv, pv, c2, nl2, nd2, key0, lim, dp);
+        else ew_pairs_dq<false>(sv, pv, c2, nl2, nd2, key0, lim, dp);
         tmem_st2_x16<64>(tB + 16 * c, dp);  // dS packed into dP's columns 64h + 16c ..
       }
       tmem_wait_st();

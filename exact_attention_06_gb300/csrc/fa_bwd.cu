@@ -140,15 +140,22 @@ __device__ __forceinline__ void issue_product(uint32_t d_tmem, uint64_t da, uint
 // already read.  Column of the k-th 16-element K block:
 __device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? 8u * kk : 64u + 8u * (kk - 4); }
 
-// G (+)= X Y with X (128 x 128) packed bf16 in TMEM (layout above) and Y a 128 x d MN-major tile.
+// G (+)= X Y with X (128 x 128) packed bf16 in TMEM (layout above) and Y a 128 x d MN-major
+// tile, half at a time: the K blocks that the elementwise threads' chunk `part` produced (chunk c
+// of the thread holding elements 64h.. writes elements 64h + 32c .. +31, i.e. K blocks
+// {0, 1, 4, 5} for c = 0 and {2, 3, 6, 7} for c = 1), so the MMAs of the first chunk run while
+// the second is computed.
 template <int D>
-__device__ __forceinline__ void issue_grad(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idesc,
-                                           bool accumulate) {
-  if (accumulate) mma_ts_c<1>(d_tmem, a_tmem, db, idesc);
-  else mma_ts_c<0>(d_tmem, a_tmem, db, idesc);
+__device__ __forceinline__ void issue_grad_part(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idesc,
+                                                bool accumulate, int part) {
 #pragma unroll
-  for (int kk = 1; kk < kTile / 16; ++kk)
-    mma_ts_c<1>(d_tmem, a_tmem + packed_col(kk), sdesc_add(db, static_cast<uint32_t>(kk) * 2048u), idesc);
+  for (int q = 0; q < 4; ++q) {
+    const int kk = 2 * part + (q & 1) + 4 * (q >> 1);
+    const uint32_t a = a_tmem + packed_col(kk);
+    const uint64_t b = sdesc_add(db, static_cast<uint32_t>(kk) * 2048u);
+    if (q == 0 && !accumulate) mma_ts_c<0>(d_tmem, a, b, idesc);
+    else mma_ts_c<1>(d_tmem, a, b, idesc);
+  }
 }
 
 // Elementwise step of the dK/dV kernel on 32 query columns of one key row (column pairs packed
@@ -211,7 +218,7 @@ struct DkdvCfg : BwdCfg<D> {
   static constexpr uint32_t OFF_VEC = OFF_RING + B::ST * STAGE;
   static constexpr uint32_t OFF_BAR = OFF_VEC + B::ST * B::VEC;
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
-                       B_DRAIN = B_PF + 1, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;  // B_PF + c: chunk c of the elementwise step
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
 };
@@ -250,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::B_SF), 1);
     mbar_init(BAR(C::B_PF), kEwWarps * 32);
+    mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
     mbar_init(BAR(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -326,11 +334,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(BAR(C::B_SF));
       }
       for (int i = 0; ok && i < n_i; ++i) {
-        if (!bwait(BAR(C::B_PF), i & 1, abort_flag, budget)) break;
-        tc_fence_after();
         const uint32_t st = (i % C::ST) * C::STAGE;
-        issue_grad<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0);  // dV += P^T dO
-        issue_grad<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0);      // dK += dS^T Q
+        bool part_ok = true;
+        for (int part = 0; part < 2; ++part) {  // each half as soon as the elementwise warps finish it
+          if (!bwait(BAR(C::B_PF + part), i & 1, abort_flag, budget)) {
+            part_ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_grad_part<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0 || part > 0,
+                             part);  // dV += P^T dO
+          issue_grad_part<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0 || part > 0,
+                             part);  // dK += dS^T Q
+        }
+        if (!part_ok) break;
         tc_commit(BAR(C::B_EMPTY + i % C::ST));
         if (i + 1 < n_i) {
           if (!bwait(BAR(C::B_FULL + (i + 1) % C::ST), ((i + 1) / C::ST) & 1, abort_flag, budget)) break;
@@ -372,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         else ew_pairs_dkdv<false>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
         tmem_st2_x16<64>(tA + 16 * c, pp);  // P^T packed: columns 64h + 16c ..
         tmem_st2_x16<64>(tB + 16 * c, dp);  // dS^T packed
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(BAR(C::B_PF));
     }
     if (ok) ok = bwait_all(BAR(C::B_SF), n_i & 1, abort_flag, budget);  // gradients final
     if (ok) {
@@ -405,7 +422,7 @@ struct DqCfg : BwdCfg<D> {
   static constexpr uint32_t STAGE = 2 * B::TB;
   static constexpr uint32_t OFF_BAR = OFF_RING + B::ST * STAGE;
   static constexpr int B_QD = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
-                       B_DRAIN = B_PF + 1, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;  // B_PF + c: chunk c of the elementwise step
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
 };
@@ -441,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::B_SF), 1);
     mbar_init(BAR(C::B_PF), kEwWarps * 32);
+    mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
     mbar_init(BAR(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -498,9 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(BAR(C::B_SF));
       }
       for (int j = 0; ok && j < n_j; ++j) {
-        if (!bwait(BAR(C::B_PF), j & 1, abort_flag, budget)) break;
-        tc_fence_after();
-        issue_grad<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, j > 0);  // dQ += dS K
+        bool part_ok = true;
+        for (int part = 0; part < 2; ++part) {  // each half as soon as the elementwise warps finish it
+          if (!bwait(BAR(C::B_PF + part), j & 1, abort_flag, budget)) {
+            part_ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g,
+                             j > 0 || part > 0, part);  // dQ += dS K
+        }
+        if (!part_ok) break;
         tc_commit(BAR(C::B_EMPTY + j % C::ST));
         if (j + 1 < n_j) {
           if (!bwait(BAR(C::B_FULL + (j + 1) % C::ST), ((j + 1) / C::ST) & 1, abort_flag, budget)) break;
@@ -540,10 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (key0 + 31 > lim) ew_pairs_dq<true>(sv, pv, c2, nl2, nd2, key0, lim, dp);
         else ew_pairs_dq<false>(sv, pv, c2, nl2, nd2, key0, lim, dp);
         tmem_st2_x16<64>(tB + 16 * c, dp);  // dS packed into dP's columns 64h + 16c ..
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(BAR(C::B_PF));
     }
     if (ok) ok = bwait_all(BAR(C::B_SF), n_j & 1, abort_flag, budget);
     if (ok) {

@@ -1,0 +1,87 @@
+"""GPU properties beyond the parity cases: bitwise determinism (no kernel uses atomics or a
+run-dependent order), extreme score magnitudes, a very long decode and a wide grid."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _util import assert_parity, ensure_built, run_fwd
+from exact_attention_06_gb300 import fattn, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_forward_is_bitwise_deterministic(d, causal):
+    q, k, v = inputs.prefill_inputs(2, 4, 1000, d, seed=d, device=DEV)
+    o1, l1 = run_fwd(q, k, v, 1 / math.sqrt(d), causal)
+    o2, l2 = run_fwd(q, k, v, 1 / math.sqrt(d), causal)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_backward_is_bitwise_deterministic():
+    B, H, N, d = 1, 4, 777, 128
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=5, device=DEV)
+    do = inputs.normal_bf16(q.shape, seed=6, device=DEV)
+    o, lse = run_fwd(q, k, v, 1 / math.sqrt(d), True)
+    grads = []
+    for _ in range(2):
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        fattn.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, 1 / math.sqrt(d), True)
+        fattn.fa_get_status()
+        grads.append((dq, dk, dv))
+    for a, b in zip(*grads):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_extreme_scores_do_not_overflow(causal):
+    # q and k scaled by 8: scaled scores reach several hundred (exp overflows fp32 past 88), so
+    # without the running max every row would overflow; rows are then nearly one-hot
+    B, H, N, d = 1, 2, 640, 128
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=12, device=DEV)
+    q, k = q * 8, k * 8  # exact in bf16 (a power of two)
+    o, lse = run_fwd(q, k, v, 1 / math.sqrt(d), causal, o_fp32=True)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(d), causal)
+    assert np.abs(lse_ref).max() > 200
+    assert_parity(o, lse, o_ref, lse_ref, "x8 scores")
+
+
+def test_decode_very_long_sequence():
+    # B1 H2 L = 262144 (2048 chunks): automatic splits, every split merged by the combine
+    B, H, L, d = 1, 2, 262144, 128
+    q, k, v = inputs.decode_inputs(B, H, L, d, seed=21, device=DEV)
+    o = torch.empty((B, H, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(fattn.fa_decode_workspace_bytes(B, H, L, d, 128, 0), dtype=torch.uint8, device=DEV)
+    fattn.fa_decode_splitkv(q, k, v, o, lse, 1 / math.sqrt(d), ws, 128, 0)
+    fattn.fa_get_status()
+    o_ref, lse_ref = oracle.decode(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(d))
+    assert_parity(o.reshape(B * H, d), lse.reshape(B * H), o_ref, lse_ref, "L=262144")
+
+
+def test_forward_wide_grid():
+    # B*H = 4096 heads of N = 200 (a ragged second tile): grid.x = 4096
+    B, H, N, d = 64, 64, 200, 64
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=33, device=DEV)
+    o, lse = run_fwd(q, k, v, 0.125, False, o_fp32=True)
+    rows = inputs.sample_rows_per_head(B, H, N, 3, seed=4)
+    picks = [(0, 0), (17, 41), (63, 63)]
+    for b, h in picks:
+        sel = rows[b, h].numpy()
+        o_ref, lse_ref = oracle.attention_head(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), 0.125, False, rows=sel)
+        got_o = o[b, h].index_select(0, rows[b, h].to(DEV))
+        got_l = lse[b, h].index_select(0, rows[b, h].to(DEV))
+        assert_parity(got_o, got_l, o_ref, lse_ref, f"b{b} h{h}")
+    # and no row anywhere is left unwritten
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())

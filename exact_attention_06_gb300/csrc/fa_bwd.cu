@@ -39,6 +39,7 @@ constexpr int kWarpMma = kEwWarps, kWarpTma = kEwWarps + 1;
 constexpr int kThreads = (kEwWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0, kColB = 128, kColG1 = 256;  // products at 0 / 128, gradients from 256
+constexpr uint32_t kColS1 = 384;  // dQ kernel: second S buffer (S(j) at kColA for even j, here for odd j)
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -504,35 +505,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);      // dS K: K MN-major
       const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dDO = sdesc_sw128(sDO, 16, 1024);
       const uint64_t dR = sdesc_sw128(sRing, 16, 1024), dRmn = sdesc_sw128(sRing, kBox, 1024);
-      auto products = [&](int j) {
+      // S(j) alternates between two TMEM buffers, so S(j+1) can run while the elementwise warps
+      // still work on step j; dP(j+1) has one buffer (dS(j) is packed into it) and follows the
+      // dQ MMAs of step j.
+      auto issue_s = [&](int j) {
         const uint32_t st = (j % C::ST) * C::STAGE;
-        issue_product<D>(tmem + kColA, dQ, sdesc_add(dR, st), idesc_p);           // S = Q K^T
+        issue_product<D>(tmem + ((j & 1) ? kColS1 : kColA), dQ, sdesc_add(dR, st), idesc_p);  // S = Q K^T
+      };
+      auto issue_dp = [&](int j) {
+        const uint32_t st = (j % C::ST) * C::STAGE;
         issue_product<D>(tmem + kColB, dDO, sdesc_add(dR, st + C::TB), idesc_p);  // dP = dO V^T
       };
       bool ok = bwait(BAR(C::B_QD), 0, abort_flag, budget) && bwait(BAR(C::B_FULL), 0, abort_flag, budget);
       if (ok) {
         tc_fence_after();
-        products(0);
+        issue_s(0);
+        issue_dp(0);
         tc_commit(BAR(C::B_SF));
       }
       for (int j = 0; ok && j < n_j; ++j) {
-        bool part_ok = true;
-        for (int part = 0; part < 2; ++part) {  // each half as soon as the elementwise warps finish it
-          if (!bwait(BAR(C::B_PF + part), j & 1, abort_flag, budget)) {
-            part_ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g,
-                             j > 0 || part > 0, part);  // dQ += dS K
-        }
-        if (!part_ok) break;
-        tc_commit(BAR(C::B_EMPTY + j % C::ST));
+        // dQ += dS K for the first chunk, then S(j+1) (under the elementwise warps' second chunk),
+        // then the second chunk's dQ MMAs and dP(j+1).
+        if (!bwait(BAR(C::B_PF), j & 1, abort_flag, budget)) break;
+        tc_fence_after();
+        issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, j > 0,
+                           0);
         if (j + 1 < n_j) {
           if (!bwait(BAR(C::B_FULL + (j + 1) % C::ST), ((j + 1) / C::ST) & 1, abort_flag, budget)) break;
           tc_fence_after();
-          products(j + 1);
+          issue_s(j + 1);
         }
+        if (!bwait(BAR(C::B_PF + 1), j & 1, abort_flag, budget)) break;
+        tc_fence_after();
+        issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, true, 1);
+        tc_commit(BAR(C::B_EMPTY + j % C::ST));
+        if (j + 1 < n_j) issue_dp(j + 1);
         tc_commit(BAR(C::B_SF));
       }
       tc_commit(BAR(C::B_DRAIN));
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * quarter + 16 * sub + (lane & 15);
     const int row = qt * kTile + r;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
-    const uint32_t tA = tmem + lane_addr + kColA, tB = tmem + lane_addr + kColB;
+    const uint32_t tB = tmem + lane_addr + kColB;  // dP; S(j) is in buffer j % 2 (kColA, kColS1)
     const bool in = row < N;
     const float lse2 = in ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : INFINITY;
     const float dd = in ? delta[static_cast<size_t>(bh) * N + row] : 0.f;
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t sv[32], pv[32];
-        tmem_ld2_x32<64>(tA + 32 * c, sv);
+        tmem_ld2_x32<64>(tmem + lane_addr + ((j & 1) ? kColS1 : kColA) + 32 * c, sv);
         tmem_ld2_x32<64>(tB + 32 * c, pv);
         uint32_t dp[16];
         const int key0 = j * kTile + 64 * h + 32 * c;

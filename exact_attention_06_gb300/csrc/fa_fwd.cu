@@ -73,18 +73,23 @@ struct FwdCfg {
                        NBAR = B_DRAIN + 2;
   // d = 64 leaves 128 TMEM columns free: P~_t gets its own columns there, so S_t(j+1) can be
   // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S.
-  static constexpr bool SEP = (D == 64) && !FP8;
-  static constexpr uint32_t COL_P = SEP ? 384u : 0u;  // + 64 t (separate) or + 128 t (aliased)
-  // At d = 64 the PV MMAs (N = 64) are too short for one issuing thread to keep the tensor core
-  // busy, so each tile gets its own MMA warp; at d = 128 one MMA warp alternating between the
-  // tiles measured faster.
-  static constexpr bool TWO_ISSUERS = (D == 64) && !FP8;
+  // E4M3 (d = 128): TMEM has no room for separate P~ columns, but shared memory has (16 KB a
+  // tile), so P~ goes there and PV reads it as an SS MMA.
+  static constexpr bool SEP = (D == 64) || FP8;
+  static constexpr bool P_SMEM = FP8;
+  static constexpr uint32_t COL_P = (SEP && !P_SMEM) ? 384u : 0u;  // + 64 t (TMEM, separate) or + 128 t (aliased)
+  static constexpr uint32_t PB = P_SMEM ? kBr * 128u : 0u;           // bytes of one tile's P~ in shared memory
+  // With separate P~ each tile gets its own MMA warp (at d = 64 the PV MMAs, N = 64, are also too
+  // short for one issuing thread); with P~ aliasing S (bf16, d = 128) one MMA warp alternating
+  // between the tiles measured faster.
+  static constexpr bool TWO_ISSUERS = SEP;
   static constexpr int WARP_TMA = kWarpMma + (TWO_ISSUERS ? 2 : 1);
   static constexpr int THREADS = (WARP_TMA + 1) * 32;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2 * QB;
   static constexpr uint32_t OFF_V = OFF_K + KST * KVB;
-  static constexpr uint32_t OFF_BAR = OFF_V + VST * KVB;
+  static constexpr uint32_t OFF_P = OFF_V + VST * KVB;       // P~ of both tiles (E4M3 only)
+  static constexpr uint32_t OFF_BAR = OFF_P + 2 * PB;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;  // TMEM address slot, abort flag
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;   // + slack to align the base to 1 KB
 };
@@ -303,31 +308,43 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     if (lane == 0) {
       const int t = warp - kWarpMma;
       const int n = t ? n_t1 : n_t0;
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
+      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(kBr, kBc, 0) : idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = FP8 ? idesc_e4m3_f32(kBr, D, 1) : idesc_bf16_f32(kBr, D, 1);
       const uint64_t dq = sdesc_add(sdesc_sw128(sQ, 16, 1024), t * C::QB);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
+      const uint64_t dp = sdesc_sw128(base + C::OFF_P + t * C::PB, 16, 1024);  // E4M3 P~: K-major, one box
       const uint32_t d_s = tmem + t * kBc;
       const uint32_t d_o = tmem + kColO + t * D;
       const uint32_t a_p = tmem + (C::SEP ? C::COL_P + 64u * t : static_cast<uint32_t>(t * kBc));
       auto issue_s = [&](int j) {
         const uint64_t dk = sdesc_add(dk0, (j % C::KST) * C::KVB);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::ROW / 32; ++kk) {  // 32 bytes of K per MMA
           const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
-          if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
-          else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          if constexpr (FP8) {
+            if (kk == 0) mma_ss_f8_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+            else mma_ss_f8_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          } else {
+            if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+            else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          }
         }
       };
       auto issue_pv = [&](int j) {
         const uint64_t dv = sdesc_add(dv0, (j % C::VST) * C::KVB);
-        if (j > 0) mma_ts_c<1>(d_o, a_p, dv, idesc_o);
-        else mma_ts_c<0>(d_o, a_p, dv, idesc_o);
 #pragma unroll
-        for (int kk = 1; kk < kBc / 16; ++kk)
-          mma_ts_c<1>(d_o, a_p + static_cast<uint32_t>(kk) * 8u, sdesc_add(dv, static_cast<uint32_t>(kk) * 2048u),
-                      idesc_o);
+        for (int kk = 0; kk < kBc / C::K_MMA; ++kk) {
+          // K_MMA keys per MMA: K_MMA rows x 128 B of each V box
+          const uint64_t b = sdesc_add(dv, static_cast<uint32_t>(kk * C::K_MMA) * 128u);
+          if constexpr (C::P_SMEM) {  // A = P~ rows in shared memory, 32 bytes (keys) per MMA
+            if (j > 0 || kk > 0) mma_ss_f8_c<1>(d_o, sdesc_add(dp, 32u * kk), b, idesc_o);
+            else mma_ss_f8_c<0>(d_o, sdesc_add(dp, 32u * kk), b, idesc_o);
+          } else {                    // A = P~ in TMEM, 8 columns (16 bf16 keys) per MMA
+            if (j > 0 || kk > 0) mma_ts_c<1>(d_o, a_p + 8u * kk, b, idesc_o);
+            else mma_ts_c<0>(d_o, a_p + 8u * kk, b, idesc_o);
+          }
+        }
       };
       auto wait = [&](uint32_t bar, uint32_t parity) {
         return mbar_wait(bar, parity, abort_flag, budget, &g_fwd_status);
@@ -534,19 +551,43 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       const float alpha = ex2(m2 - mb);
       const uint64_t nmb2 = f2_pack(-mb, -mb);
       uint64_t rs_a = f2_pack(0.f, 0.f), rs_b = rs_a;
+      float inv_ps = 1.f;  // FP8: the row sum below is of p * ps; l takes p
       if constexpr (C::SEP) {
-        // P~ packed in place into sr[0..31] (entry i holds keys 64h + 2i, 2i + 1).
+        if constexpr (FP8) {
+          // P~ as E4M3 of p * ps, ps = 256 * sv_j / sv_max (<= 256): the V block scale rides on P~
+          // so that U accumulates in one unit for every key tile.  ps is folded into the exponent:
+          // p * ps = 2^(s c - m + log2 ps).  Packed in place into sr[0..15] (entry i: keys 64h + 4i ..).
+          const float ps = 256.f * sv_j / sv_max;
+          inv_ps = sv_max / (256.f * sv_j);
+          const float lps = log2f(ps);
+          const uint64_t nmp2 = f2_pack(lps - mb, lps - mb);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2,
-                    x3);
-          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          rs_a = f2_add(rs_a, f2_pack(p0, p1));
-          rs_b = f2_add(rs_b, f2_pack(p2, p3));
-          sr[i] = pack_bf16(p0, p1);
-          sr[i + 1] = pack_bf16(p2, p3);
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2, nmp2), x0,
+                      x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2, nmp2), x2,
+                      x3);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            rs_a = f2_add(rs_a, f2_pack(p0, p1));
+            rs_b = f2_add(rs_b, f2_pack(p2, p3));
+            sr[i] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+        } else {
+          // P~ packed in place into sr[0..31] (entry i holds keys 64h + 2i, 2i + 1).
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0,
+                      x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2,
+                      x3);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            rs_a = f2_add(rs_a, f2_pack(p0, p1));
+            rs_b = f2_add(rs_b, f2_pack(p2, p3));
+            sr[i] = pack_bf16(p0, p1);
+            sr[i + 1] = pack_bf16(p2, p3);
+          }
         }
         // PV_t(j-1) must be done before P~_t(j) overwrites P~_t(j-1) and before U_t is rescaled.
         if (j > 0) {
@@ -555,36 +596,24 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           tc_fence_after();
           if (!__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
         }
-        uint32_t pr[32];
+        if constexpr (C::P_SMEM) {
+          // row r of this tile's P~ (128 E4M3 keys = 128 bytes, 128-byte swizzle); this thread's
+          // keys 64h .. 64h + 63 are 16-byte chunks 4h .. 4h + 3
+          const uint32_t prow = base + C::OFF_P + t * C::PB + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pr[i] = sr[i];
-        tmem_st2_x32<32>(t_p, pr);
-      }
-      float inv_ps = 1.f;  // FP8: the row sum below is of p * ps; l takes p
-      if constexpr (FP8) {
-        // P~ as E4M3 of p * ps, ps = 256 * sv_j / sv_max (<= 256): the V block scale rides on P~
-        // so that U accumulates in one unit for every key tile; 4 keys per TMEM column.  ps is
-        // folded into the exponent: p * ps = 2^(s c - m + log2 ps).
-        const float ps = 256.f * sv_j / sv_max;
-        inv_ps = sv_max / (256.f * sv_j);
-        const float lps = log2f(ps);
-        const uint64_t nmp2 = f2_pack(lps - mb, lps - mb);
-        uint32_t pr[16];
+          for (int i = 0; i < 4; ++i)
+            sts128(prow + ((static_cast<uint32_t>(4 * h + i) ^ static_cast<uint32_t>(r & 7)) << 4), sr[4 * i],
+                   sr[4 * i + 1], sr[4 * i + 2], sr[4 * i + 3]);
+          fence_proxy_async_smem();  // the PV MMA reads it through the async proxy
+        } else {
+          uint32_t pr[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2, nmp2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2, nmp2), x2,
-                    x3);
-          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          rs_a = f2_add(rs_a, f2_pack(p0, p1));
-          rs_b = f2_add(rs_b, f2_pack(p2, p3));
-          pr[i] = pack_e4m3x4(p0, p1, p2, p3);
+          for (int i = 0; i < 32; ++i) pr[i] = sr[i];
+          tmem_st2_x32<32>(t_p, pr);
         }
-        tmem_st2_x16<16>(t_s, pr);  // keys 64h + 4i .. +3 -> column 16h + i
       }
 #pragma unroll
-      for (int q = 0; q < ((C::SEP || FP8) ? 0 : 2); ++q) {
+      for (int q = 0; q < (C::SEP ? 0 : 2); ++q) {
         uint32_t pr[16];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {

@@ -59,12 +59,15 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.447e6,
-                                "sha256": "b2f4f95f98efaf4c389795b5f65d8526a6c81ca12e0817fc538828c77851f327"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 587.789e6,
-                               "sha256": "b2f4f95f98efaf4c389795b5f65d8526a6c81ca12e0817fc538828c77851f327"},
-    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 199.790e6,
-                                   "sha256": "b2f4f95f98efaf4c389795b5f65d8526a6c81ca12e0817fc538828c77851f327"},
+    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.633e6,
+                                "sha256": "01443c5e011d05af785909acde3251b7ad70d7e3181a2c7fa95abba7550d829a"},
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 588.102e6,
+                               "sha256": "01443c5e011d05af785909acde3251b7ad70d7e3181a2c7fa95abba7550d829a"},
+    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 217.222e6,
+                                   "sha256": "01443c5e011d05af785909acde3251b7ad70d7e3181a2c7fa95abba7550d829a"},
+    # backward: the dominant kernel (dK/dV) on the causal workload
+    ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1047.634e6,
+                                    "sha256": "208eadff17955d1b0a7ede7c25dee933060383e41355730a0af1970b6029767a"},
     # decode: captured on the B4 slice (decode_small) and scaled by 16 to B64 (K/V streamed once)
     ("decode_split_kernel", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2151.272e6,
                                         "sha256": "f5a79caa980ce126dce15dbfcad29b01d9650f5ef0e0a34ba9b96520a131e5e1"},
@@ -448,8 +451,9 @@ def run_ours(args):
             "value": round(bflops / (bt * 1e-3) / 1e12 * world, 3), "unit": "TFLOP/s", "ms_per_step": round(bt, 4),
             "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
             "config": {"B": wb.B, "H": wb.H, "N": wb.N, "d": wb.d, "causal": True, "spike_every_64th_key_x8": True},
-            "roofline": _roofline("tensor", bflops, bt, peaks, None),
-            "note": "fa_bwd: rowsum(O*dO), dK/dV pass, dQ pass; flops = 2.5 x forward (algorithmic)"}
+            "roofline": _roofline("tensor", bflops, bt, peaks, _traffic("bwd_dkdv_kernel", "causal")),
+            "note": "fa_bwd: rowsum(O*dO), dK/dV pass, dQ pass; flops = 2.5 x forward (algorithmic); "
+                    "traffic is the dominant dK/dV kernel's"}
         del bst
         torch.cuda.empty_cache()
         # split-KV decode over a paged cache (128-key pages, shuffled pool) on the decode workload

@@ -59,12 +59,12 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.633e6,
-                                "sha256": "01443c5e011d05af785909acde3251b7ad70d7e3181a2c7fa95abba7550d829a"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 588.102e6,
-                               "sha256": "01443c5e011d05af785909acde3251b7ad70d7e3181a2c7fa95abba7550d829a"},
-    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 217.222e6,
-                                   "sha256": "01443c5e011d05af785909acde3251b7ad70d7e3181a2c7fa95abba7550d829a"},
+    ("fwd_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.032e6,
+                                "sha256": "f6b72efdf5e529523f69e6ca8a586ed7b23362ec67e4462fb0760a1e4cf96df2"},
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 587.917e6,
+                               "sha256": "f6b72efdf5e529523f69e6ca8a586ed7b23362ec67e4462fb0760a1e4cf96df2"},
+    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 215.731e6,
+                                   "sha256": "f6b72efdf5e529523f69e6ca8a586ed7b23362ec67e4462fb0760a1e4cf96df2"},
     # backward: the dominant kernel (dK/dV) on the causal workload
     ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1047.634e6,
                                     "sha256": "208eadff17955d1b0a7ede7c25dee933060383e41355730a0af1970b6029767a"},

@@ -22,14 +22,21 @@
 //              (iceferryling "FlashAttention 1 和 FlashAttention 2 的区别", §7-8
 //              split-Q).  They also apply the alpha rescale of U_0 and write O_0, lse.
 //   warps 8-15 the same for Q_1.
-//   warp 16    MMA issuer (one thread) and TMEM owner.
-//   warp 17    TMA producer: Q_0, Q_1 once, then K_j and V_j into two rings.
-// The tensor core alternates between the tiles: [PV_0(j-1), S_0(j)] runs while
-// the Q_1 softmax works on S_1(j-1), and [PV_1(j-1), S_1(j)] while the Q_0
-// softmax works on S_0(j).  The commit after S_t(j) also covers PV_t(j-1), so
-// the softmax that sees S_t(j) may rescale U_t in place.
-// TMEM columns: S_0/P~_0 at 0, S_1/P~_1 at 128 (P~ as packed bf16 in the first
-// 64 columns of its S), U_0 at 256, U_1 at 256 + d.
+//   MMA warp(s) one issuing thread each; the first also owns TMEM.
+//   last warp  TMA producer: Q_0, Q_1 once, then K_j and V_j into two rings.
+// Three schedules, by where P~ lives:
+//   bf16, d = 128: TMEM holds S_0, S_1 (columns 0, 128) and U_0, U_1 (256, 384), so
+//     P~ is written as packed bf16 into the first 64 columns of its own S.  One MMA
+//     warp alternates between the tiles: [PV_0(j-1), S_0(j)] runs while the Q_1
+//     softmax works on S_1(j-1) and vice versa; the commit after S_t(j) also covers
+//     PV_t(j-1), so the softmax that sees S_t(j) may rescale U_t in place.
+//   bf16, d = 64: U_t takes 64 columns, so P~_t gets its own TMEM columns
+//     (384 + 64t) and one MMA warp per tile issues S_t(j+1) as soon as the softmax
+//     has read S_t(j) ("separate P~"); the softmax waits for PV_t(j-1) only before
+//     overwriting P~_t and rescaling U_t.
+//   E4M3, d = 128: TMEM is laid out as for bf16 d = 128, but shared memory has room
+//     for P~ (16 KB a tile): the separate-P~ schedule with P~ in shared memory, read
+//     by the PV MMA as an SS operand.
 //
 // Causal: key tiles above a query tile's diagonal are never computed for it
 // (Q_0 stops one tile before Q_1); only the diagonal tile masks (col > row ->
@@ -399,26 +406,19 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   } else if (!C::TWO_ISSUERS && warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer for both tiles
     if constexpr (!C::TWO_ISSUERS) if (lane == 0) {
-      // S = Q K^T (both K-major); U += P V (V MN-major).  bf16: kind::f16; FP8: kind::f8f6f4, E4M3.
-      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(kBr, kBc, 0) : idesc_bf16_f32(kBr, kBc, 0);
-      constexpr uint32_t idesc_o = FP8 ? idesc_e4m3_f32(kBr, D, 1) : idesc_bf16_f32(kBr, D, 1);
+      // bf16, d = 128 (P~ aliasing S).  S = Q K^T (both K-major); U += P~ V (V MN-major).
+      static_assert(!FP8 && !C::SEP, "one MMA warp for both tiles only with P~ aliasing S (bf16)");
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
       // Descriptors computed once; each MMA below is one 32-bit add plus the tcgen05.mma.
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
       auto mma_s = [&](bool acc, uint32_t d, uint64_t a, uint64_t b) {
-        if constexpr (FP8) {
-          if (acc) mma_ss_f8_c<1>(d, a, b, idesc_s); else mma_ss_f8_c<0>(d, a, b, idesc_s);
-        } else {
-          if (acc) mma_ss_c<1>(d, a, b, idesc_s); else mma_ss_c<0>(d, a, b, idesc_s);
-        }
+        if (acc) mma_ss_c<1>(d, a, b, idesc_s); else mma_ss_c<0>(d, a, b, idesc_s);
       };
       auto mma_o = [&](bool acc, uint32_t d, uint32_t a, uint64_t b) {
-        if constexpr (FP8) {
-          if (acc) mma_ts_f8_c<1>(d, a, b, idesc_o); else mma_ts_f8_c<0>(d, a, b, idesc_o);
-        } else {
-          if (acc) mma_ts_c<1>(d, a, b, idesc_o); else mma_ts_c<0>(d, a, b, idesc_o);
-        }
+        if (acc) mma_ts_c<1>(d, a, b, idesc_o); else mma_ts_c<0>(d, a, b, idesc_o);
       };
       auto issue_s = [&](int t, int j) {
         const uint64_t dq = sdesc_add(dq0, t * C::QB);
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       };
       auto issue_pv = [&](int t, int j) {
         const uint64_t dv = sdesc_add(dv0, (j % C::VST) * C::KVB);
-        const uint32_t a_p = tmem + (C::SEP ? C::COL_P + 64u * t : static_cast<uint32_t>(t * kBc));
+        const uint32_t a_p = tmem + static_cast<uint32_t>(t * kBc);
         const uint32_t d_o = tmem + kColO + t * D;
         // K_MMA keys per MMA: K_MMA rows x 128 B of each V box (boxes kBox apart along d);
         // the P~ operand advances 8 TMEM columns (32 bytes of each row) per MMA.
@@ -454,7 +454,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           }
         tc_commit(BAR(C::B_KE));
       }
-      static_assert(!C::SEP, "the separate-P~ schedule runs with an MMA warp per tile");
       for (int j = 1; ok && j <= n_max; ++j) {
         // This iteration's operands first (V_{j-1} for the PVs, K_j for the next S; both are
         // normally loaded long before), so that once a tile's P~ is ready its 2x(ROW/32) MMAs

@@ -7,8 +7,10 @@ One JSON line on rank 0.  The headline workload is the prefill configuration
 (fa_fwd) over it, timed with CUDA events on the launching stream, L2 flushed
 (256 MiB write) between timed steps because its inputs (50 MB) fit in L2.
 ``extra`` carries the other workloads of the target (causal N=8192 d=128 with
-x8 key spikes, ragged causal N=16381, split-KV decode L=32768), each with its
-roofline fraction; their inputs exceed L2.  ``e2e`` repeats the headline
+x8 key spikes, ragged causal N=16381, split-KV decode L=32768) and of the
+library's further paths (backward and FP8 forward on the causal workload, the
+decode over a paged cache, the causal workload in four key shards merged by the
+combine), each with its roofline fraction; their inputs exceed L2.  ``e2e`` repeats the headline
 through the C ABI with pinned host buffers and the host<->device copies
 inside the timed region.  ``cpu_baseline`` is the fp64 oracle timed on the
 host cores over a bounded sample.  ``--impl reference`` times that oracle

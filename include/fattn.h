@@ -1,6 +1,9 @@
 /*
- * libfattn -- exact fused attention forward and split-KV decode for GB300
- * (sm_103a).  C ABI: plain pointers, sizes and a stream handle.
+ * libfattn -- exact fused attention for GB300 (sm_103a): the fused forward
+ * (bf16, or E4M3 inputs with block scales), its backward, a split-KV decode
+ * (contiguous or paged KV cache), the log-sum-exp combine of partials and a
+ * forward over one key shard.  C ABI: plain pointers, sizes and a stream
+ * handle.
  *
  * What is computed (per batch b and head h, scores scaled by `scale`):
  *     S = scale * Q K^T,   P = softmax(S) row-wise,   O = P V,
@@ -24,7 +27,7 @@
  *     returns an error status, writes nothing and launches nothing.  No C++
  *     exception crosses this boundary.  There is no CPU fallback and no
  *     other backend: an unsupported request is an error.
- *   - Supported head dimensions: d = 64 and d = 128.
+ *   - Supported head dimensions: d = 64 and d = 128 (the FP8 forward: 128).
  *   - Device: compute capability 10.3 (GB300).  Anything else gives
  *     FA_ERR_ARCH.
  */

@@ -72,9 +72,11 @@ design notes):
   §4; triton-tutorial §8.4.5).  The cnblogs page's block-local normalisation
   gives the same result.
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_backward_pins.py`` against values the pages print, closed
-forms, invariants, a library routine and brute force.
+Every function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_oracle_backward_pins.py``, ``tests/test_oracle_fp8_pins.py`` and
+``tests/test_oracle_paged_pins.py`` against values the pages print, closed
+forms, invariants, library routines (torch's float8 conversion and fp64 SDPA)
+and brute force.
 """
 
 from __future__ import annotations

@@ -3,8 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One JSON line on rank 0.  The headline workload is the prefill configuration
-(B=4, H=16, N=2048, d=64, non-causal, bf16): one step is one fused forward
-(fa_fwd) over it, timed with CUDA events on the launching stream, L2 flushed
+(B=4, H=16, N=2048, d=64, non-causal, bf16): one step is one fa_fwd_ex call over
+it (the fused forward; its 512 blocks of 256 query rows fill 3.37 waves of the
+152 SMs, so the last wave's blocks are split along the keys and a combine kernel
+merges them), timed with CUDA events on the launching stream, L2 flushed
 (256 MiB write) between timed steps because its inputs (50 MB) fit in L2.
 ``extra`` carries the other workloads of the target (causal N=8192 d=128 with
 x8 key spikes, ragged causal N=16381, split-KV decode L=32768) and of the
@@ -185,10 +187,20 @@ def _prefill_step_fn(w, dev, stream):
     q, k, v = inputs.workload_inputs(w, seed=0, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    ws = _tail_workspace(w, dev)
 
     def step():
-        fattn.fa_fwd(q, k, v, o, lse, w.scale, w.causal, stream=stream)
-    return step, 1
+        fattn.fa_fwd_ex(q, k, v, o, lse, w.scale, w.causal, stream=stream, workspace=ws)
+    return step, 1 if ws is None else 2
+
+
+def _tail_workspace(w, dev):
+    """The forward's tail-split workspace for this workload on this device (None: no split
+    planned, one launch; otherwise the forward and the combine of the split blocks)."""
+    import torch
+    from exact_attention_06_gb300 import fattn
+    nbytes = fattn.fa_fwd_workspace_bytes(w.B, w.H, w.N, w.d, w.causal)
+    return torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
 
 
 def _decode_step_fn(w, dev, stream):
@@ -357,13 +369,14 @@ def _e2e_prefill(w, dev, stream, steps, warmup):
     qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
     od = torch.empty_like(qd)
     ld = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    ws = _tail_workspace(w, dev)
 
     def step():
         with torch.cuda.stream(stream):
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
-            fattn.fa_fwd(qd, kd, vd, od, ld, w.scale, w.causal, stream=stream)
+            fattn.fa_fwd_ex(qd, kd, vd, od, ld, w.scale, w.causal, stream=stream, workspace=ws)
             oh.copy_(od, non_blocking=True)
             lh.copy_(ld, non_blocking=True)
 
@@ -526,7 +539,9 @@ def run_ours(args):
                    "causal": w.causal, "scale": w.scale, "global_batch": w.B * world, "seq_len": w.N,
                    "parallelism": f"replicas x{world}", "l2": "flushed between timed steps (256 MiB write)"},
         "gpu_launches": launches * args.steps,
-        "roofline": _roofline("tensor", flops, t_local, peaks, _traffic("fwd_kernel", HEADLINE)),
+        "roofline": dict(_roofline("tensor", flops, t_local, peaks, _traffic("fwd_kernel", HEADLINE)),
+                         note="duration covers the forward kernel and, when the tail is split, the combine "
+                              "kernel; traffic is the forward kernel's"),
         "clocks": sampler.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kThreads)
 #define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_launch();  // the combine may launch once every split CTA has started
   const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(splits));
   const int sp = static_cast<int>(blockIdx.x % static_cast<unsigned>(splits));
   int* page_ids = reinterpret_cast<int*>(gbase + C::OFF_PAGES);
@@ -310,57 +312,88 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // One warp per row, kCombineRows rows per CTA: lane l holds columns [l*D/32, (l+1)*D/32).
-// The row's partial maxima are read 32 at a time (one per lane) and reduced by shuffles; then
-// each partial's U slice is one vector load per lane.  Empty partials (m = -inf) are skipped
-// without reading their U or l.
+// With at most kCombineFast partials (every split-KV decode of a few splits, the forward's tail
+// split) each lane issues all its loads at once -- the row's m and l (the same address in every
+// lane) and one vector of each partial's U -- and then merges; an empty partial (m = -inf) gets
+// weight 0 and its U and l, whatever they hold, are not used.  More partials: the maxima are
+// read 32 at a time (one per lane) and reduced by shuffles, then the partials are merged one by
+// one, an empty one without reading its U or l.
 constexpr int kCombineRows = 8;
+constexpr int kCombineFast = 8;
 
-template <int D>
+template <int D, bool OF32>
 __global__ void __launch_bounds__(32 * kCombineRows)
     combine_kernel(const float* __restrict__ u_part, const float* __restrict__ m_part,
-                   const float* __restrict__ l_part, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int R,
-                   int S) {
+                   const float* __restrict__ l_part, void* __restrict__ o, float* __restrict__ lse, int R, int S) {
   constexpr int C = D / 32;  // columns per lane: 2 or 4
+  using VecC = typename std::conditional<C == 4, float4, float2>::type;
   const int lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * kCombineRows + (threadIdx.x >> 5);
+  grid_dep_wait();  // launched programmatically after the kernel that writes the partials
   if (r >= R) return;
   const float* mr = m_part + r * S;
   const float* lr = l_part + r * S;
   const float* ur = u_part + r * S * D + lane * C;
-  float mm = -INFINITY;
-  for (int s = lane; s < S; s += 32) mm = fmaxf(mm, mr[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
-  float lt = 0.f, acc[C];
+  float mm = -INFINITY, lt = 0.f, acc[C];
 #pragma unroll
   for (int i = 0; i < C; ++i) acc[i] = 0.f;
-  if (mm != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float ms = mr[s];
-      if (ms == -INFINITY) continue;  // empty partial: weight 0, U and l not read
-      const float w = expf(ms - mm);
-      lt = fmaf(w, lr[s], lt);
-      if constexpr (C == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(ur + static_cast<size_t>(s) * D);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
-        acc[2] = fmaf(w, x.z, acc[2]);
-        acc[3] = fmaf(w, x.w, acc[3]);
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(ur + static_cast<size_t>(s) * D);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
+  auto add = [&](float w, const VecC& x) {
+    acc[0] = fmaf(w, x.x, acc[0]);
+    acc[1] = fmaf(w, x.y, acc[1]);
+    if constexpr (C == 4) {
+      acc[2] = fmaf(w, x.z, acc[2]);
+      acc[3] = fmaf(w, x.w, acc[3]);
+    }
+  };
+  if (S <= kCombineFast) {
+    float ms[kCombineFast], ls[kCombineFast];
+    VecC us[kCombineFast];
+#pragma unroll
+    for (int s = 0; s < kCombineFast; ++s)
+      if (s < S) {
+        ms[s] = mr[s];
+        ls[s] = lr[s];
+        us[s] = *reinterpret_cast<const VecC*>(ur + static_cast<size_t>(s) * D);
+        mm = fmaxf(mm, ms[s]);
+      }
+    if (mm != -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < kCombineFast; ++s)
+        if (s < S && ms[s] != -INFINITY) {
+          const float w = expf(ms[s] - mm);
+          lt = fmaf(w, ls[s], lt);
+          add(w, us[s]);
+        }
+    }
+  } else {
+    for (int s = lane; s < S; s += 32) mm = fmaxf(mm, mr[s]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+    if (mm != -INFINITY) {
+      for (int s = 0; s < S; ++s) {
+        const float ms = mr[s];
+        if (ms == -INFINITY) continue;  // empty partial: weight 0, U and l not read
+        const float w = expf(ms - mm);
+        lt = fmaf(w, lr[s], lt);
+        add(w, *reinterpret_cast<const VecC*>(ur + static_cast<size_t>(s) * D));
       }
     }
   }
   const float inv = lt > 0.f ? 1.f / lt : 0.f;
-  __nv_bfloat16* orow = o + r * D + lane * C;
-  if constexpr (C == 4) {
+  if constexpr (OF32) {
+    float* orow = static_cast<float*>(o) + r * D + lane * C;
+    if constexpr (C == 4)
+      *reinterpret_cast<float4*>(orow) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    else
+      *reinterpret_cast<float2*>(orow) = make_float2(acc[0] * inv, acc[1] * inv);
+  } else if constexpr (C == 4) {
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(o) + r * D + lane * C;
     uint2 w2;
     w2.x = pack_bf16(acc[0] * inv, acc[1] * inv);
     w2.y = pack_bf16(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(orow) = w2;
   } else {
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(o) + r * D + lane * C;
     *reinterpret_cast<uint32_t*>(orow) = pack_bf16(acc[0] * inv, acc[1] * inv);
   }
   if (lane == 0) lse[r] = lt > 0.f ? mm + logf(lt) : -INFINITY;
@@ -388,15 +421,23 @@ cudaError_t launch_decode_split(const DecodeLaunch& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
-                           int S, int d, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>((R + kCombineRows - 1) / kCombineRows);
+                           int S, int d, int o_fp32, cudaStream_t stream) {
+  // Programmatic launch: the combine's CTAs may be scheduled while the kernel before it finishes
+  // (they wait in grid_dep_wait), which hides its launch latency.
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>((R + kCombineRows - 1) / kCombineRows));
+  cfg.blockDim = dim3(32 * kCombineRows);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
   if (d == 64)
-    combine_kernel<64><<<grid, 32 * kCombineRows, 0, stream>>>(u_part, m_part, l_part,
-                                                               static_cast<__nv_bfloat16*>(o), lse, R, S);
-  else
-    combine_kernel<128><<<grid, 32 * kCombineRows, 0, stream>>>(u_part, m_part, l_part,
-                                                                static_cast<__nv_bfloat16*>(o), lse, R, S);
-  return cudaGetLastError();
+    return o_fp32 ? cudaLaunchKernelEx(&cfg, combine_kernel<64, true>, u_part, m_part, l_part, o, lse, R, S)
+                  : cudaLaunchKernelEx(&cfg, combine_kernel<64, false>, u_part, m_part, l_part, o, lse, R, S);
+  return o_fp32 ? cudaLaunchKernelEx(&cfg, combine_kernel<128, true>, u_part, m_part, l_part, o, lse, R, S)
+                : cudaLaunchKernelEx(&cfg, combine_kernel<128, false>, u_part, m_part, l_part, o, lse, R, S);
 }
 
 // Scratch for fa_decode_splitkv_noalloc: the per-split partials live here

@@ -38,11 +38,20 @@
 //     for P~ (16 KB a tile): the separate-P~ schedule with P~ in shared memory, read
 //     by the PV MMA as an SS operand.
 //
+// Two kernels share these schedules.  fwd_kernel runs one CTA per block of 256 query rows
+// (causal launches order the blocks longest first).  fwd_persist_kernel (non-causal bf16,
+// d = 64) runs one CTA per SM that walks a list of blocks, keeping TMEM, barriers and the K/V
+// ring between them, so that a block's Q load and first S overlap the previous block's last
+// steps and epilogue; it also runs the key pieces of fa_fwd_ex's tail split.
+//
 // Causal: key tiles above a query tile's diagonal are never computed for it
 // (Q_0 stops one tile before Q_1); only the diagonal tile masks (col > row ->
 // -inf), and the ragged last tile masks col >= N (triton-tutorial §8.7.1
 // STAGE split; xuesongtap §2.2 last paragraph).
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <climits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -75,9 +84,9 @@ struct FwdCfg {
   static constexpr int VST = FP8 ? 4 : ((D == 128) ? 2 : 4);  // V ring stages
   static constexpr uint32_t QB = NH * kBox;         // bytes of one Q tile
   static constexpr uint32_t KVB = NH * kBox;        // bytes of one K (or V) tile
-  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
+  static constexpr int B_Q = 0, B_QE = B_Q + 1, B_KF = B_QE + 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
                        B_SF = B_VE + VST, B_PF = B_SF + 2, B_SC = B_PF + 2, B_OF = B_SC + 2, B_DRAIN = B_OF + 2,
-                       NBAR = B_DRAIN + 2;
+                       B_OSF = B_DRAIN + 2, B_OW = B_OSF + 2, NBAR = B_OW + 2;
   // d = 64 leaves 128 TMEM columns free: P~_t gets its own columns there, so S_t(j+1) can be
   // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S.
   // E4M3 (d = 128): TMEM has no room for separate P~ columns, but shared memory has (16 KB a
@@ -100,8 +109,14 @@ struct FwdCfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;  // TMEM address slot, abort flag
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;   // + slack to align the base to 1 KB
 };
+// The persistent kernel (bf16 d = 64) adds O of both tiles, staged for the TMA store (128 bytes a row).
+struct PersistSmem {
+  static constexpr uint32_t OFF_O = (FwdCfg<64>::OFF_MISC + 16u + 1023u) & ~1023u;
+  static constexpr uint32_t SMEM = OFF_O + 2u * kBr * 128u + 1024u;
+};
 static_assert(FwdCfg<128>::SMEM <= 232448, "shared memory of the d=128 kernel exceeds 227 KB");
 static_assert(FwdCfg<128, true>::SMEM <= 232448, "shared memory of the FP8 kernel exceeds 227 KB");
+static_assert(PersistSmem::SMEM <= 232448, "shared memory of the persistent kernel exceeds 227 KB");
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long budget) {
@@ -174,14 +189,13 @@ __device__ __forceinline__ void store_half_row(void* o, float* lse, size_t row_o
 // exp(s - m)), m in natural-log units, l; an empty row (no admissible key) gets m = -inf,
 // l = 0 and no U.
 template <int D>
-__device__ __forceinline__ void store_half_partial(const FwdAux& aux, size_t prow, int h, bool valid, uint32_t taddr,
+__device__ __forceinline__ void store_half_partial(const FwdAux& aux, size_t slot, int h, bool valid, uint32_t taddr,
                                                    float l, float m2, bool have_u) {
   uint32_t ur[D / 2];
   if (have_u) {
     if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
   }
   if (!valid) return;
-  const size_t slot = prow * aux.S + aux.shard;
   const bool empty = !(l > 0.f);
   if (!empty) {  // an empty partial's U is never read (the combine skips m = -inf)
     float4* dst = reinterpret_cast<float4*>(aux.u_part + slot * D + h * (D / 2));
@@ -218,6 +232,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 #define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_launch();  // a dependent kernel may launch once every CTA has started
   const int bh = blockIdx.x;
   const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest causal work first
   const int n_tiles = (Nk + kBc - 1) / kBc;
@@ -256,6 +271,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  // Set-up above may overlap the previous kernel in the stream (programmatic launch); every
+  // global access below comes after it has completed.
+  grid_dep_wait();
   if constexpr (FP8) {
     if (warp == 1) {  // the head's largest V block scale (P~ is quantized relative to it)
       float mv = 0.f;
@@ -264,10 +286,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       for (int off = 16; off > 0; off >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
       if (lane == 0) *sv_max_slot = mv;
     }
-  }
-  if (warp == kWarpMma) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -648,13 +666,15 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       tc_fence_after();
       const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
       if (aux.u_part)
-        store_half_partial<D>(aux, static_cast<size_t>(bh) * N + row, h, row < N, t_o, l_row, m2, true);
+        store_half_partial<D>(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, h, row < N, t_o, l_row,
+                              m2, true);
       else
         store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
                           FP8 ? sv_max * (1.f / 256.f) : 1.f);
     } else if (aux.u_part && n == 0) {
       // no key of this shard is admissible for the tile: an empty partial, U never touched
-      store_half_partial<D>(aux, static_cast<size_t>(bh) * N + row, h, row < N, t_o, 0.f, -INFINITY, false);
+      store_half_partial<D>(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, h, row < N, t_o, 0.f,
+                            -INFINITY, false);
     }
     tmem_wait_st();
   }
@@ -667,17 +687,455 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Persistent forward for non-causal bf16 at d = 64: one CTA per SM walks its work items
+// (blockIdx.x, + gridDim.x, ...).  An item is a block of 256 query rows (two tiles) of one (b, h)
+// against the keys koff .. koff + Nk - 1, loaded from key row kload; the blocks run in
+// (b*h, block) order, and with the tail split (aux.lin) the blocks from n_full on are cut into
+// ksplit key pieces that leave partial (U, m, l) rows for the combine kernel.  Between items a
+// CTA keeps its TMEM, barriers and K/V ring: the next Q is loaded as soon as the last S MMAs of
+// the current item have read Q, and the next item's S(0) is issued right after the current
+// item's last PV, under the softmax warps' epilogue.  The step itself is the separate-P~
+// schedule of fwd_kernel at d = 64.
+struct FwdItem {
+  int bh, pair, koff, kload, Nk, n0, n1;
+  bool to_part;
+  long long srow0;  // partial slot of flat row r (= b*h*N + n): (r - srow0) * smul + sadd
+  int smul, sadd;
+};
+
+__device__ __forceinline__ FwdItem item_at(int w, const FwdAux& aux, int N) {
+  FwdItem I;
+  I.koff = aux.koff;
+  I.kload = 0;
+  I.Nk = aux.Nk;
+  I.to_part = aux.u_part != nullptr && !aux.lin;
+  I.srow0 = 0;
+  I.smul = aux.S;
+  I.sadd = aux.shard;
+  const int n_pairs = (N + kRowsPerCta - 1) / kRowsPerCta;
+  int u = w;
+  if (aux.lin && w >= aux.n_full) {
+    const int piece = w - aux.n_full;
+    u = aux.n_full + piece / aux.ksplit;
+    I.sadd = piece % aux.ksplit;
+    I.koff = I.kload = I.sadd * aux.kchunk;
+    I.Nk = min(aux.kchunk, N - I.koff);
+    I.to_part = true;
+    I.srow0 = aux.prow0;
+    I.smul = aux.ksplit;
+  }
+  I.bh = u / n_pairs;
+  I.pair = u % n_pairs;
+  const int n_tiles = (I.Nk + kBc - 1) / kBc;
+  I.n0 = n_tiles;  // tile 0 of a block is inside N
+  I.n1 = I.pair * kRowsPerCta + kBr < N ? n_tiles : 0;
+  return I;
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    fwd_persist_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, void* __restrict__ o, float* __restrict__ lse,
+                       int N, float sl2, int o_fp32, unsigned long long budget, const FwdAux aux,
+                       const __grid_constant__ CUtensorMap to) {
+  using C = FwdCfg<D>;
+  static_assert(D == 64 && C::SEP && C::TWO_ISSUERS && !C::P_SMEM, "the persistent forward is the d = 64 schedule");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sBar = base + C::OFF_BAR;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+#define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_launch();  // a dependent kernel (the tail combine) may launch once every CTA has started
+  const int w0 = static_cast<int>(blockIdx.x), w_step = static_cast<int>(gridDim.x), n_items = aux.n_items;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_Q), 1);
+    mbar_init(BAR(C::B_QE), 2);
+    // Each K (V) stage is released once by each tile's MMA warp; a tile with no rows in an item
+    // releases the item's stages without reading them.
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(BAR(C::B_KF + s), 1);
+      mbar_init(BAR(C::B_KE + s), 2);
+    }
+    for (int s = 0; s < C::VST; ++s) {
+      mbar_init(BAR(C::B_VF + s), 1);
+      mbar_init(BAR(C::B_VE + s), 2);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(C::B_SF + t), 1);
+      mbar_init(BAR(C::B_PF + t), kSoftmaxWarps * 32);
+      mbar_init(BAR(C::B_SC + t), kSoftmaxWarps * 32);
+      mbar_init(BAR(C::B_OF + t), 1);
+    }
+    mbar_init(BAR(C::B_DRAIN), 1);
+    mbar_init(BAR(C::B_DRAIN + 1), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(C::B_OSF + t), 1);                 // O staging of tile t free again
+      mbar_init(BAR(C::B_OW + t), kSoftmaxWarps * 32);  // O staging of tile t written
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  grid_dep_wait();  // as in fwd_kernel: global accesses only after the previous kernel completed
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // Barrier phases run on across a CTA's items: K/V stage g of the ring is the CTA's g-th key
+  // tile, the per-tile barriers count that tile's steps over all items, and Q's the items.
+
+  if (warp == C::WARP_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      int k_issued = 0, v_issued = 0, q_issued = 0, kc = 0;
+      bool ok = true;
+      for (int w = w0, it = 0; ok && w < n_items; w += w_step, ++it) {
+        const FwdItem I = item_at(w, aux, N);
+        const int n_max = I.n0;
+        // The previous item's Q is free once both tiles' last S MMAs have completed.
+        if (it > 0 && !mbar_wait(BAR(C::B_QE), (it - 1) & 1, abort_flag, budget, &g_fwd_status)) break;
+        mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QB);
+        for (int t = 0; t < 2; ++t)
+          for (int h = 0; h < C::NH; ++h)
+            tma_load_3d(sQ + t * C::QB + h * kBox, &tq, BAR(C::B_Q), h * C::BOX_X, I.pair * kRowsPerCta + t * kBr,
+                        I.bh);
+        q_issued = it + 1;
+        for (int j = 0; j < n_max; ++j) {
+          const int g = kc + j;
+          const int ks = g % C::KST;
+          if (g >= C::KST &&
+              !mbar_wait(BAR(C::B_KE + ks), ((g / C::KST) - 1) & 1, abort_flag, budget, &g_fwd_status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(BAR(C::B_KF + ks), C::KVB);
+          for (int h = 0; h < C::NH; ++h)
+            tma_load_3d(sK + ks * C::KVB + h * kBox, &tk, BAR(C::B_KF + ks), h * C::BOX_X, I.kload + j * kBc, I.bh);
+          k_issued = g + 1;
+          const int vs = g % C::VST;
+          if (g >= C::VST &&
+              !mbar_wait(BAR(C::B_VE + vs), ((g / C::VST) - 1) & 1, abort_flag, budget, &g_fwd_status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(BAR(C::B_VF + vs), C::KVB);
+          for (int h = 0; h < C::NH; ++h)
+            tma_load_3d(sV + vs * C::KVB + h * kBox, &tv, BAR(C::B_VF + vs), h * C::BOX_X, I.kload + j * kBc, I.bh);
+          v_issued = g + 1;
+        }
+        kc += n_max;
+      }
+      // Every copy this CTA started must land before its shared memory is released (a Q load is
+      // issued only after the previous one was consumed, so only the last can be in flight).
+      if (q_issued > 0) drain_wait(BAR(C::B_Q), (q_issued - 1) & 1, budget);
+      for (int g = max(0, k_issued - C::KST); g < k_issued; ++g)
+        drain_wait(BAR(C::B_KF + g % C::KST), (g / C::KST) & 1, budget);
+      for (int g = max(0, v_issued - C::VST); g < v_issued; ++g)
+        drain_wait(BAR(C::B_VF + g % C::VST), (g / C::VST) & 1, budget);
+    }
+  } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+    // ------------------------------------------------------------ MMA issuer of one tile
+    if (lane == 0) {
+      const int t = warp - kWarpMma;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
+      const uint64_t dq = sdesc_add(sdesc_sw128(sQ, 16, 1024), t * C::QB);
+      const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
+      const uint32_t d_s = tmem + t * kBc;
+      const uint32_t d_o = tmem + kColO + t * D;
+      const uint32_t a_p = tmem + C::COL_P + 64u * t;
+      auto issue_s = [&](int g) {  // S_t = Q_t K^T with K from ring stage g
+        const uint64_t dk = sdesc_add(dk0, (g % C::KST) * C::KVB);
+#pragma unroll
+        for (int kk = 0; kk < C::ROW / 32; ++kk) {  // 32 bytes of K per MMA
+          const uint32_t off = static_cast<uint32_t>(kk & 3) * 32u;
+          if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+        }
+      };
+      auto issue_pv = [&](int g, bool first) {  // U_t (+)= P~_t V with V from ring stage g
+        const uint64_t dv = sdesc_add(dv0, (g % C::VST) * C::KVB);
+#pragma unroll
+        for (int kk = 0; kk < kBc / C::K_MMA; ++kk) {  // 16 keys per MMA: 8 TMEM columns of P~
+          const uint64_t b = sdesc_add(dv, static_cast<uint32_t>(kk * C::K_MMA) * 128u);
+          if (!first || kk > 0) mma_ts_c<1>(d_o, a_p + 8u * kk, b, idesc_o);
+          else mma_ts_c<0>(d_o, a_p + 8u * kk, b, idesc_o);
+        }
+      };
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        return mbar_wait(bar, parity, abort_flag, budget, &g_fwd_status);
+      };
+      int g = 0, kc = 0;  // this tile's steps and the CTA's key tiles over the items so far
+      bool ok = true, issued = false;
+      for (int w = w0, it = 0; ok && w < n_items; w += w_step, ++it) {
+        const FwdItem I = item_at(w, aux, N);
+        const int n = t ? I.n1 : I.n0, n_max = I.n0;
+        // This item's Q (waited for first in every case, so that this warp's release of Q below
+        // falls into this item's phase).
+        ok = wait(BAR(C::B_Q), it & 1);
+        if (!ok) break;
+        if (n == 0) {  // no rows of this tile in the item: release Q and every K/V stage unread
+          mbar_arrive(BAR(C::B_QE));
+          for (int j = 0; ok && j < n_max; ++j) {
+            const int gg = kc + j;
+            ok = wait(BAR(C::B_KF + gg % C::KST), (gg / C::KST) & 1);
+            if (ok) mbar_arrive(BAR(C::B_KE + gg % C::KST));
+            ok = ok && wait(BAR(C::B_VF + gg % C::VST), (gg / C::VST) & 1);
+            if (ok) mbar_arrive(BAR(C::B_VE + gg % C::VST));
+          }
+          kc += n_max;
+          continue;
+        }
+        // The previous item's last S read by the softmax, and this item's first K.
+        ok = (g == 0 || wait(BAR(C::B_SC + t), (g - 1) & 1)) && wait(BAR(C::B_KF + kc % C::KST), (kc / C::KST) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(kc);
+        issued = true;
+        tc_commit(BAR(C::B_SF + t));
+        tc_commit(BAR(C::B_KE + kc % C::KST));
+        if (n == 1) tc_commit(BAR(C::B_QE));  // the item's last S
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n) {  // S_t(j+1) as soon as the softmax has read S_t(j)
+            const int gk = kc + j + 1;
+            ok = wait(BAR(C::B_SC + t), (g + j) & 1) && wait(BAR(C::B_KF + gk % C::KST), (gk / C::KST) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(gk);
+            tc_commit(BAR(C::B_SF + t));
+            tc_commit(BAR(C::B_KE + gk % C::KST));
+            if (j + 2 == n) tc_commit(BAR(C::B_QE));
+          }
+          const int gv = kc + j;
+          ok = wait(BAR(C::B_PF + t), (g + j) & 1) && wait(BAR(C::B_VF + gv % C::VST), (gv / C::VST) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(gv, j == 0);
+          tc_commit(BAR(C::B_OF + t));
+          tc_commit(BAR(C::B_VE + gv % C::VST));
+        }
+        g += n;
+        kc += n_max;
+      }
+      if (issued) {  // all MMAs complete before TMEM is released
+        tc_commit(BAR(C::B_DRAIN + t));
+        drain_wait(BAR(C::B_DRAIN + t), 0, budget);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps 0-15
+    const int t = warp / kSoftmaxWarps;           // query tile of this warp
+    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+    const int sub = (warp % kSoftmaxWarps) >> 2;  // which 16 lanes of the quarter
+    const int h = lane >> 4;                      // which half of the row's columns
+    const int r = 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
+    const uint32_t t_s = tmem + lane_addr + static_cast<uint32_t>(t * kBc);
+    const uint32_t t_o = tmem + lane_addr + kColO + static_cast<uint32_t>(t * D);
+    const uint32_t t_p = tmem + lane_addr + C::COL_P + 64u * t;
+    const uint64_t c2 = f2_pack(sl2, sl2);
+    // bf16 O leaves through shared memory and one TMA store per tile and item, issued by the
+    // tile's first thread; fp32 O and partials are stored by each thread.
+    const bool o_issuer = (warp % kSoftmaxWarps) == 0 && lane == 0;
+    const uint32_t o_stage = base + PersistSmem::OFF_O + static_cast<uint32_t>(t) * (kBr * 128u);
+    int g = 0;   // this tile's steps over the items so far: the phases of its SF and OF barriers
+    int gi = 0;  // this tile's O tiles staged so far: the phases of its OSF and OW barriers
+    bool ok = true;
+    for (int w = w0; ok && w < n_items; w += w_step) {
+      const FwdItem I = item_at(w, aux, N);
+      const int n = t ? I.n1 : I.n0;
+      // The staging is free once the previous store has read it (long done by now); one phase
+      // per item whose O is staged.
+      if (o_issuer && n > 0 && !o_fp32 && !I.to_part) {
+        bulk_wait_read_all();
+        mbar_arrive(BAR(C::B_OSF + t));
+      }
+      const int row = I.pair * kRowsPerCta + t * kBr + r;
+      const int lim = I.Nk - 1;  // last key of the item (local index)
+      float m2 = -INFINITY, l = 0.f;  // l: this thread's half of the row
+      for (int j = 0; ok && j < n; ++j) {
+        ok = wait_all(BAR(C::B_SF + t), (g + j) & 1, abort_flag, budget);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_SC + t));  // S_t(j) is in registers: the MMA may overwrite it
+        const int nvalid = lim - j * kBc - 64 * h + 1;  // keys of the item among them
+        if (nvalid < 64) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
+        }
+        float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
+        float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int i = 4; i < 60; i += 8) {
+          a0 = fmax3(a0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+          a1 = fmax3(a1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+          a2 = fmax3(a2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+          a3 = fmax3(a3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+        }
+        a0 = fmax3(a0, __uint_as_float(sr[60]), __uint_as_float(sr[61]));
+        a1 = fmax3(a1, __uint_as_float(sr[62]), __uint_as_float(sr[63]));
+        float mx = fmax3(a0, a1, fmaxf(a2, a3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // join the two halves of the row
+        const float m_new = fmaxf(m2, mx * sl2);
+        const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
+        const float alpha = ex2(m2 - mb);
+        const uint64_t nmb2 = f2_pack(-mb, -mb);
+        uint64_t rs_a = f2_pack(0.f, 0.f), rs_b = rs_a;
+        // P~ packed in place into sr[0..31] (entry i holds keys 64h + 2i, 2i + 1).
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2,
+                    x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          rs_a = f2_add(rs_a, f2_pack(p0, p1));
+          rs_b = f2_add(rs_b, f2_pack(p2, p3));
+          sr[i] = pack_bf16(p0, p1);
+          sr[i + 1] = pack_bf16(p2, p3);
+        }
+        // PV_t(j-1) must be done before P~_t(j) overwrites P~_t(j-1) and before U_t is rescaled
+        // (for j = 0 the previous item's epilogue waited for its last PV).
+        if (j > 0) {
+          ok = wait_all(BAR(C::B_OF + t), (g + j - 1) & 1, abort_flag, budget);
+          if (!ok) break;
+          tc_fence_after();
+          if (!__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
+        }
+        {
+          uint32_t pr[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pr[i] = sr[i];
+          tmem_st2_x32<32>(t_p, pr);
+        }
+        float s0, s1, s2, s3;
+        f2_unpack(rs_a, s0, s1);
+        f2_unpack(rs_b, s2, s3);
+        l = fmaf(alpha, l, (s0 + s1) + (s2 + s3));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PF + t));
+        m2 = m_new;
+      }
+      if (!ok) break;
+      if (n == 0) continue;  // the tile is past N: nothing to write
+      ok = wait_all(BAR(C::B_OF + t), (g + n - 1) & 1, abort_flag, budget);  // U_t final
+      if (!ok) break;
+      g += n;
+      tc_fence_after();
+      const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      // (the item is decoded again here rather than kept live through the steps)
+      const FwdItem E = item_at(w, aux, N);
+      const long long frow = static_cast<long long>(E.bh) * N + row;
+      if (E.to_part) {
+        store_half_partial<D>(aux, static_cast<size_t>(frow - E.srow0) * E.smul + E.sadd, h, row < N, t_o, l_row, m2,
+                              true);
+      } else if (o_fp32) {
+        store_half_row<D>(o, lse, static_cast<size_t>(frow), h, row < N, true, t_o, l_row, m2, 1.f);
+      } else {
+        // Row r of the staged tile: 128 bytes (64 bf16), 16-byte chunk c at chunk c ^ (r & 7)
+        // (the 128-byte swizzle of the O map); this thread's columns 32h .. 32h + 31 are chunks
+        // 4h .. 4h + 3.  Rows past N are staged too; the store does not write them.
+        uint32_t ur[32];
+        tmem_ld2_x32<32>(t_o, ur);
+        const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
+        if (h == 0 && row < N) lse[frow] = (l_row > 0.f) ? (m2 + log2f(l_row)) * kLn2 : -INFINITY;
+        ok = wait_all(BAR(C::B_OSF + t), gi & 1, abort_flag, budget);
+        if (!ok) break;
+        const uint32_t srow = o_stage + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t* u = ur + 8 * i;
+          sts128(srow + ((static_cast<uint32_t>(4 * h + i) ^ static_cast<uint32_t>(r & 7)) << 4),
+                 pack_bf16(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
+                 pack_bf16(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
+                 pack_bf16(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
+                 pack_bf16(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
+        }
+        fence_proxy_async_smem();  // the TMA store reads the staging through the async proxy
+        mbar_arrive(BAR(C::B_OW + t));
+        if (o_issuer) {
+          ok = mbar_wait(BAR(C::B_OW + t), gi & 1, abort_flag, budget, &g_fwd_status);
+          if (ok) {
+            tma_store_3d(&to, o_stage, 0, E.pair * kRowsPerCta + t * kBr, E.bh);
+            bulk_commit();
+          }
+        }
+        ++gi;
+      }
+      // The U_t loads above complete (tcgen05.wait::ld) before this thread's first P~-ready
+      // arrival of the next item, after which PV_t(0) of that item may overwrite U_t.
+    }
+    if (o_issuer) bulk_wait_all();  // the stores complete before the CTA exits
+  }
+#undef BAR
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// One launch of `kern` (a forward kernel) with programmatic stream serialization: its set-up may
+// overlap the previous kernel in the stream.
+template <typename Kern, typename... Args>
+cudaError_t launch_kernel(Kern kern, dim3 grid, int threads, uint32_t smem, cudaStream_t stream, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D, bool CAUSAL, bool FP8 = false>
 cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
-  auto kern = fwd_kernel<D, CAUSAL, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
-  if (e != cudaSuccess) return e;
   const int n_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
-  dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.o, a.lse, a.N, a.scale_log2, a.o_fp32, a.budget,
-                                              a.aux);
-  return cudaGetLastError();
+  FwdAux aux = a.aux;
+  if constexpr (!CAUSAL && !FP8 && D == 64) {
+    // the persistent kernel: one CTA per SM over the work items
+    const long long units = static_cast<long long>(a.BH) * n_pairs;
+    const long long items = aux.lin ? aux.n_full + (units - aux.n_full) * aux.ksplit : units;
+    if (items > INT_MAX) return cudaErrorInvalidValue;
+    aux.n_items = static_cast<int>(items);
+    const dim3 grid(static_cast<unsigned>(a.sms > 0 ? std::min<long long>(items, a.sms) : items));
+    return launch_kernel(fwd_persist_kernel<D>, grid, C::THREADS, PersistSmem::SMEM, stream, a.tq, a.tk, a.tv, a.o,
+                         a.lse, a.N, a.scale_log2, a.o_fp32, a.budget, aux, a.to);
+  } else {
+    // one CTA per block of 256 query rows (the tail split is planned for the persistent kernel only)
+    if (aux.lin) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
+    return launch_kernel(fwd_kernel<D, CAUSAL, FP8>, grid, C::THREADS, C::SMEM, stream, a.tq, a.tk, a.tv, a.o, a.lse,
+                         a.N, a.scale_log2, a.o_fp32, a.budget, aux);
+  }
 }
 
 }  // namespace

@@ -171,6 +171,55 @@ fa_status_t plan_paged(int B, int H, int L, int d, int page_size, int splits, in
   return plan_decode(B, H, L, d, 128, (n_chunks + chunks_per_split - 1) / chunks_per_split, 0, plan);
 }
 
+// Tail split of the non-causal d = 64 forward.  With one resident CTA per SM, U blocks of 256 query
+// rows run in ceil(U / sms) waves, the last holding rem blocks.  Cutting each of those rem blocks
+// into k key pieces (>= 2 key tiles each) spreads the last wave over k * rem CTAs, whose partial
+// (U, m, l) rows the combine kernel then merges.  Costs are counted in key-tile steps: a CTA's
+// prologue and epilogue about 2 steps, the combine about 1.5.  A split is taken when it saves at
+// least 5 % of the whole launch.
+struct TailPlan {
+  int ksplit = 1;  // 1: no split
+  int n_full = 0, kchunk = 0;
+  long long prow0 = 0, rows = 0;
+  size_t u_bytes = 0, m_bytes = 0, l_bytes = 0;
+  size_t total() const { return u_bytes + m_bytes + l_bytes; }
+};
+
+TailPlan plan_tail(long long bh, int N, int d, int causal, int sms) {
+  TailPlan p;
+  if (causal || d != 64 || sms < 1) return p;  // the persistent d = 64 kernel runs the pieces
+  const long long n_pairs = (N + 255) / 256;
+  const long long U = bh * n_pairs;
+  const int n_tiles = (N + 127) / 128;
+  const long long waves = (U + sms - 1) / sms;
+  const long long rem = U - (waves - 1) * sms;
+  constexpr double kFixed = 2.0, kCombine = 1.5;
+  const double t_whole = n_tiles + kFixed;
+  double best_t = t_whole;
+  int best_k = 1, best_tpp = n_tiles;
+  for (int k = 2; k <= 8 && 2 * k <= n_tiles; ++k) {
+    const int tpp = (n_tiles + k - 1) / k;  // key tiles per piece
+    if ((n_tiles + tpp - 1) / tpp != k) continue;
+    const double t = std::ceil(static_cast<double>(k * rem) / sms) * (tpp + kFixed) + kCombine;
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best_k = k;
+      best_tpp = tpp;
+    }
+  }
+  if (best_k == 1 || t_whole - best_t < 0.05 * waves * t_whole) return p;
+  if (U - rem + rem * best_k > INT_MAX) return p;
+  p.ksplit = best_k;
+  p.kchunk = best_tpp * 128;
+  p.n_full = static_cast<int>(U - rem);
+  p.prow0 = (p.n_full / n_pairs) * N + (p.n_full % n_pairs) * 256;
+  p.rows = bh * N - p.prow0;
+  p.u_bytes = round256(static_cast<size_t>(p.rows) * best_k * d * sizeof(float));
+  p.m_bytes = round256(static_cast<size_t>(p.rows) * best_k * sizeof(float));
+  p.l_bytes = p.m_bytes;
+  return p;
+}
+
 fa_status_t check_paged_args(int B, int H, int d, int page_size, int max_pages, int num_pages, int max_seq_len) {
   if (B < 1 || H < 1) return fail(FA_ERR_INVALID_ARG, "B and H must be >= 1 (got %d, %d)", B, H);
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
@@ -221,13 +270,23 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   const long long bh = static_cast<long long>(B) * H;
   if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
   if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 query-tile grid limit", N);
-  fa_status_t st = check_device(nullptr);
+  int sms = 0;
+  fa_status_t st = check_device(&sms);
   if (st != FA_OK) return st;
+  void* ws = opts ? opts->workspace : nullptr;
+  const TailPlan tail = ws ? plan_tail(bh, N, d, causal, sms) : TailPlan{};
+  if (tail.ksplit > 1) {
+    if (opts->workspace_bytes < tail.total())
+      return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes fa_fwd_workspace_bytes gives",
+                  opts->workspace_bytes, tail.total());
+    if (!aligned(ws, 256)) return fail(FA_ERR_INVALID_ARG, "opts->workspace must be 256-byte aligned");
+  }
 
   fattn::FwdLaunch a{};
   if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tk, k, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tv, v, d, N, bh, 128)) != FA_OK) return st;
+  if (!o_fp32 && (st = make_map(&a.to, o, d, N, bh, 128)) != FA_OK) return st;
   a.o = o;
   a.lse = lse;
   a.N = N;
@@ -238,10 +297,36 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   a.scale_log2 = scale * 1.4426950408889634f;
   a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
   a.aux.Nk = N;
+  a.sms = sms;
+  if (tail.ksplit > 1) {
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    a.aux.lin = 1;
+    a.aux.n_full = tail.n_full;
+    a.aux.ksplit = tail.ksplit;
+    a.aux.kchunk = tail.kchunk;
+    a.aux.prow0 = tail.prow0;
+    a.aux.u_part = reinterpret_cast<float*>(w);
+    a.aux.m_part = reinterpret_cast<float*>(w + tail.u_bytes);
+    a.aux.l_part = reinterpret_cast<float*>(w + tail.u_bytes + tail.m_bytes);
+  }
   cudaGetLastError();  // clear a stale, non-sticky error so that it is not blamed on this launch
-  cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fattn::launch_fwd(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+  if (tail.ksplit > 1) {
+    uint8_t* o_tail = static_cast<uint8_t*>(o) + static_cast<size_t>(tail.prow0) * d * (o_fp32 ? 4 : 2);
+    e = fattn::launch_combine(a.aux.u_part, a.aux.m_part, a.aux.l_part, o_tail, lse + tail.prow0,
+                              static_cast<int>(tail.rows), tail.ksplit, d, o_fp32, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd tail combine launch");
+  }
   return FA_OK;
+}
+
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1)) return 0;
+  int sms = 0;
+  if (check_device(&sms) != FA_OK) return 0;
+  return plan_tail(static_cast<long long>(B) * H, N, d, causal, sms).total();
 }
 
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -267,9 +352,11 @@ fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u
   const long long bh = static_cast<long long>(B) * H;
   if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
   if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 query-tile grid limit", N);
-  fa_status_t st = check_device(nullptr);
+  int sms = 0;
+  fa_status_t st = check_device(&sms);
   if (st != FA_OK) return st;
   fattn::FwdLaunch a{};
+  a.sms = sms;
   if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tk, k, d, Nk, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tv, v, d, Nk, bh, 128)) != FA_OK) return st;
@@ -413,7 +500,7 @@ fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fattn::launch_decode_split(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv split launch");
-  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, s);
+  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv combine launch");
   return FA_OK;
 }
@@ -519,7 +606,7 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fattn::launch_decode_split(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged split launch");
-  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, s);
+  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged combine launch");
   return FA_OK;
 }
@@ -536,7 +623,7 @@ fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_
   fa_status_t st = check_device(nullptr);
   if (st != FA_OK) return st;
   cudaGetLastError();
-  cudaError_t e = fattn::launch_combine(u_part, m_part, l_part, o, lse, R, S, d, static_cast<cudaStream_t>(stream));
+  cudaError_t e = fattn::launch_combine(u_part, m_part, l_part, o, lse, R, S, d, 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_combine launch");
   return FA_OK;
 }

@@ -29,10 +29,22 @@ struct FwdAux {
   float* m_part;
   float* l_part;
   int shard, S;
+  // Tail split (lin = 1): a 1-D grid of work items over 256-row query blocks in (b*h, block)
+  // order.  Items [0, n_full) are whole blocks writing O and lse; each later block is split
+  // into ksplit key pieces of kchunk keys (items n_full + ksplit*(block - n_full) + piece),
+  // and piece s of flat row r (= b*h*N + n) writes partial slot (r - prow0) * ksplit + s.
+  int lin;
+  int n_full;
+  int ksplit;
+  int kchunk;
+  long long prow0;
+  // Persistent CTAs (non-causal bf16): the number of work items; set by launch_fwd.
+  int n_items;
 };
 
 struct FwdLaunch {
   CUtensorMap tq, tk, tv;
+  CUtensorMap to;  // bf16 O as {d, N, B*H} (persistent kernel's TMA store; unused for fp32 O and partials)
   void* o;
   float* lse;
   int N;
@@ -43,6 +55,7 @@ struct FwdLaunch {
   float scale_log2;  // scale * log2(e)
   unsigned long long budget;
   int fp8;            // 1: q, k, v are E4M3 with per-128-row block scales in aux (d = 128)
+  int sms;            // SMs of the device: the persistent grid size (0: one CTA per work item)
   FwdAux aux;
 };
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
@@ -75,7 +88,7 @@ constexpr int kMaxSplitPages = 1024;  // page ids one split of the paged decode 
 constexpr int kDecodeCtasPerSm = 2;   // resident split CTAs per SM (shared-memory bound)
 cudaError_t launch_decode_split(const DecodeLaunch& a, cudaStream_t stream);
 cudaError_t launch_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse,
-                           int R, int S, int d, cudaStream_t stream);
+                           int R, int S, int d, int o_fp32, cudaStream_t stream);
 unsigned int decode_read_and_clear_status();
 
 // Backward launch description: q, k, v, dO as 3-D tensors {d, N, B*H} with

@@ -25,7 +25,7 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
             "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes", "fa_decode_paged",
             "fa_combine", "fa_get_status", "fa_status_string",
             "fa_last_error")
@@ -39,7 +39,8 @@ class FattnError(RuntimeError):
 
 
 class FaFwdOpts(ctypes.Structure):
-    _fields_ = [("o_fp32", ctypes.c_int), ("wait_budget_cycles", ctypes.c_ulonglong)]
+    _fields_ = [("o_fp32", ctypes.c_int), ("wait_budget_cycles", ctypes.c_ulonglong),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
+        L.fa_fwd_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.fa_fwd_workspace_bytes.restype = sz
         L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp]
         L.fa_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, i, vp]
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
@@ -118,16 +121,24 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def fa_fwd_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool = False) -> int:
+    """Scratch bytes of fa_fwd_ex's tail split on the current device (0: no split planned)."""
+    return int(lib().fa_fwd_workspace_bytes(B, H, N, d, int(bool(causal))))
+
+
 def fa_fwd_ex(q, k, v, o, lse, scale: float, causal: bool = False, stream=None, o_fp32: bool | None = None,
-              wait_budget_cycles: int = 0):
+              wait_budget_cycles: int = 0, workspace=None):
     """Fused forward: q, k, v, o [B, H, N, d]; lse [B, H, N] fp32.
 
-    ``o`` may be bf16 (default) or fp32 (``o_fp32``, inferred from o's dtype).
+    ``o`` may be bf16 (default) or fp32 (``o_fp32``, inferred from o's dtype).  ``workspace``:
+    an optional uint8 CUDA tensor of at least fa_fwd_workspace_bytes() bytes for the tail split.
     """
     B, H, N, d = q.shape
     if o_fp32 is None:
         o_fp32 = o.dtype == torch.float32
-    opts = FaFwdOpts(int(bool(o_fp32)), int(wait_budget_cycles))
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    opts = FaFwdOpts(int(bool(o_fp32)), int(wait_budget_cycles), _ptr(workspace) if workspace is not None else None,
+                     ws_bytes)
     st = lib().fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
                          _stream(stream), ctypes.byref(opts))
     _check(st, "fa_fwd_ex")

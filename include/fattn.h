@@ -54,6 +54,9 @@ typedef enum {
 typedef struct {
   int o_fp32;                            /* 0: O is bf16 (round to nearest even); 1: O is fp32 */
   unsigned long long wait_budget_cycles; /* per-wait spin budget in SM clock cycles; 0 = default (about 2 s) */
+  void* workspace;                       /* optional device scratch, 256-byte aligned, for the tail split
+                                            (fa_fwd_workspace_bytes); NULL: one launch, no split */
+  size_t workspace_bytes;                /* its size in bytes */
 } fa_fwd_opts;
 
 /*
@@ -81,10 +84,28 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
                    int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /* fa_fwd with options (opts may be NULL).  With opts->o_fp32 = 1, `o` is an
- * fp32 [B, H, N, d] tensor. */
+ * fp32 [B, H, N, d] tensor.
+ *
+ * Tail split (non-causal, d = 64): the forward works on blocks of 256 query
+ * rows of a (b, h), one block per SM at a time, so when the last round of
+ * blocks only partly fills the SMs most of them idle through it.  Given a
+ * workspace of fa_fwd_workspace_bytes() bytes, the blocks of that last round
+ * are instead split along the keys into pieces
+ * that each leave a partial (U, m, l) per row, and a second kernel merges them
+ * by the online-softmax rule, as the split-KV decode does (FlashDecoding
+ * split-K, cnblogs jzssuanfa page, §三 场景 B).  O and lse are the same
+ * function of q, k, v up to rounding order.  With a workspace too small for
+ * the plan: FA_ERR_WORKSPACE. */
 fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                       int B, int H, int N, int d, float scale, int causal, void* stream,
                       const fa_fwd_opts* opts);
+
+/* fa_fwd_workspace_bytes -- scratch bytes the tail split of fa_fwd_ex needs on
+ * the current device for this problem, or 0 when it plans no split (causal
+ * launches, d = 128, last waves that are nearly full, fewer than 4 key tiles,
+ * invalid sizes, no sm_103a device).  The plan depends on the device's SM
+ * count. */
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal);
 
 /*
  * fa_fwd_partial -- the forward over one shard of the keys, leaving a partial
@@ -102,7 +123,7 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
  *   m_part,  [B*H*N, S] fp32, 4-byte aligned: slot `shard` gets m (the row max
  *   l_part   of the scaled scores, natural-log units) and l = sum_j exp(s_j - m).
  *            A row with no admissible key in the shard gets m = -inf and
- *            l = 0; its U slot is left as it was (fa_combine does not read it).
+ *            l = 0; its U slot is left as it was (fa_combine does not use it).
  *   causal   1: query i attends global keys j <= i (top-left aligned).
  *   d in {64, 128}; 0 <= shard < S; key_offset >= 0; other arguments as fa_fwd.
  * After one call per shard (any order, any stream order that completes them
@@ -142,7 +163,8 @@ fa_status_t fa_quantize_e4m3(const void* x, void* codes, float* scales,
  *   o           [B, H, N, d] bf16 (fp32 with opts->o_fp32), 16-byte aligned.
  *   lse         [B, H, N] fp32 (written), as for fa_fwd.
  *   d           must be 128 (FA_ERR_UNSUPPORTED otherwise).
- *   scale, causal, opts: as for fa_fwd_ex (opts may be NULL).
+ *   scale, causal, opts: as for fa_fwd_ex (opts may be NULL; no tail split:
+ *               opts->workspace is not used).
  * Scores are S = (q8 k8^T) * sq_i * sk_j * scale in fp32; P~ of key tile j
  * is stored as E4M3 of p * 256 * sv_j / max_j(sv_j) (p <= 1 after the row
  * max is subtracted), so that P~ V8 accumulates in one unit for every key
@@ -271,7 +293,7 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
  *   u_part [R, S, d] fp32, unnormalised numerators (relative to exp(s - m_s)).
  *   m_part [R, S] fp32, row maxima in natural-log units of scaled scores.
  *   l_part [R, S] fp32, denominators.
- *   An empty partial (m = -inf) has weight 0 and its U and l are not read;
+ *   An empty partial (m = -inf) has weight 0 and its U and l are not used;
  *   a row whose partials are all empty gets O = 0 and lse = -inf.
  *   o [R, d] bf16 (written), lse [R] fp32 (written).  R, S >= 1, d in {64, 128}.
  *   u_part 16-byte aligned; m_part, l_part, lse 4-byte aligned; o 16-byte aligned.

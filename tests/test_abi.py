@@ -70,6 +70,15 @@ def test_forward_argument_checks_need_no_gpu(lib):
     assert "aligned" in fattn.fa_last_error() or "N=" in fattn.fa_last_error()
 
 
+def test_forward_workspace_query_without_a_split(lib):
+    # invalid sizes and causal launches plan no split (with or without a device)
+    lib.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.fa_fwd_workspace_bytes(0, 1, 2048, 64, 0) == 0
+    assert lib.fa_fwd_workspace_bytes(1, 1, 2048, 96, 0) == 0
+    assert lib.fa_fwd_workspace_bytes(1, 1, 2048, 64, 2) == 0
+    assert lib.fa_fwd_workspace_bytes(4, 16, 2048, 64, 1) == 0
+
+
 def test_decode_workspace_sizes(lib):
     from exact_attention_06_gb300 import fattn
     # explicit splits need no device: R*S*d floats + R*S + R*S floats, each rounded up to 256 bytes

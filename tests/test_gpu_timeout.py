@@ -22,21 +22,30 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
-def test_wait_budget_expiry_is_reported_and_the_context_survives(d, causal):
+# (d, causal, O dtype, tail split): the persistent d = 64 kernel with fp32 O (stored by each
+# thread) and with bf16 O (the staged TMA store) plus the tail split's key pieces and combine;
+# the one-block-per-CTA kernel at d = 128 causal
+@pytest.mark.parametrize("d,causal,o_fp32,tail", [(64, False, True, False), (64, False, False, True),
+                                                  (128, True, True, False)])
+def test_wait_budget_expiry_is_reported_and_the_context_survives(d, causal, o_fp32, tail):
     ensure_built()
     B, H, N = 1, 4, 2000
     q, k, v = inputs.prefill_inputs(B, H, N, d, seed=21, device=DEV)
     scale = 1.0 / math.sqrt(d)
-    o = torch.zeros(B, H, N, d, dtype=torch.float32, device=DEV)
+    o = torch.zeros(B, H, N, d, dtype=torch.float32 if o_fp32 else torch.bfloat16, device=DEV)
     lse = torch.zeros(B, H, N, dtype=torch.float32, device=DEV)
-    fattn.fa_fwd_ex(q, k, v, o, lse, scale, causal, o_fp32=True, wait_budget_cycles=1)
+    ws = None
+    if tail:
+        nbytes = fattn.fa_fwd_workspace_bytes(B, H, N, d, causal)
+        assert nbytes > 0
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    fattn.fa_fwd_ex(q, k, v, o, lse, scale, causal, wait_budget_cycles=1, workspace=ws)
     with pytest.raises(fattn.FattnError) as err:
         fattn.fa_get_status()
     assert err.value.status == fattn.FA_ERR_TIMEOUT
     assert fattn.fa_get_status() == fattn.FA_OK  # the status word was cleared by the read
     # the same context still computes correct results
-    o2, lse2 = run_fwd(q, k, v, scale, causal, o_fp32=True)
+    o2, lse2 = run_fwd(q, k, v, scale, causal, o_fp32=o_fp32)
     o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), scale, causal,
                                       rows=inputs.sample_rows(N, 256, seed=1).numpy())
     rows = inputs.sample_rows(N, 256, seed=1)

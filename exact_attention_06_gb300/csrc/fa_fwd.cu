@@ -210,11 +210,38 @@ __device__ __forceinline__ void store_half_partial(const FwdAux& aux, size_t slo
   }
 }
 
+// This thread's half of an O row = U / l as bf16 into a staged O tile for the TMA store, and
+// lse from the h = 0 thread.  The tile is D/64 boxes of 128 rows x 128 bytes with the 128-byte
+// swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); the thread's D/2 columns are chunks
+// 4h .. 4h + 3 of the one box at D = 64 and all 8 chunks of box h at D = 128.  Every lane runs
+// the TMEM load (it is warp-collective); rows past N are staged too (the store skips them).
+template <int D>
+__device__ __forceinline__ void stage_half_row(uint32_t stage, float* lse, size_t row_off, int r, int h, bool valid,
+                                               uint32_t taddr, float l, float m2) {
+  uint32_t ur[D / 2];
+  if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
+  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  if (h == 0 && valid) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
+  const uint32_t srow = (D == 128 ? stage + static_cast<uint32_t>(h) * kBox : stage) + static_cast<uint32_t>(r) * 128u;
+  const int c0 = D == 128 ? 0 : 4 * h;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    const uint32_t* u = ur + 8 * i;
+    sts128(srow + ((static_cast<uint32_t>(c0 + i) ^ static_cast<uint32_t>(r & 7)) << 4),
+           pack_bf16(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
+           pack_bf16(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
+           pack_bf16(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
+           pack_bf16(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
+  }
+  fence_proxy_async_smem();  // the TMA store reads the staging through the async proxy
+}
+
 template <int D, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, void* __restrict__ o, float* __restrict__ lse, int N,
-               float sl2, int o_fp32, unsigned long long budget, const FwdAux aux) {
+               float sl2, int o_fp32, unsigned long long budget, const FwdAux aux,
+               const __grid_constant__ CUtensorMap to) {
   using C = FwdCfg<D, FP8>;
   const float* __restrict__ sq = aux.sq;
   const float* __restrict__ sk = aux.sk;
@@ -268,6 +295,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     }
     mbar_init(BAR(C::B_DRAIN), 1);
     mbar_init(BAR(C::B_DRAIN + 1), 1);
+    mbar_init(BAR(C::B_OW), kSoftmaxWarps * 32);  // O of tile t staged (bf16 O)
+    mbar_init(BAR(C::B_OW + 1), kSoftmaxWarps * 32);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -665,12 +694,26 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
-      if (aux.u_part)
+      if (aux.u_part) {
         store_half_partial<D>(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, h, row < N, t_o, l_row,
                               m2, true);
-      else
+      } else if (!FP8 && !o_fp32) {
+        // bf16 O through shared memory: Q_t's buffer is free (tile t's S MMAs are complete) and
+        // has the O tile's shape; its first thread stores it with TMA once all 256 have written.
+        const uint32_t stage = sQ + static_cast<uint32_t>(t) * C::QB;
+        stage_half_row<D>(stage, lse, static_cast<size_t>(bh) * N + row, r, h, row < N, t_o, l_row, m2);
+        mbar_arrive(BAR(C::B_OW + t));
+        if ((warp % kSoftmaxWarps) == 0 && lane == 0 &&
+            mbar_wait(BAR(C::B_OW + t), 0, abort_flag, budget, &g_fwd_status)) {
+          for (int hb = 0; hb < C::NH; ++hb)
+            tma_store_3d(&to, stage + static_cast<uint32_t>(hb) * kBox, hb * 64, pair * kRowsPerCta + t * kBr, bh);
+          bulk_commit();
+          bulk_wait_all();  // complete before the CTA exits
+        }
+      } else {
         store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
                           FP8 ? sv_max * (1.f / 256.f) : 1.f);
+      }
     } else if (aux.u_part && n == 0) {
       // no key of this shard is admissible for the tile: an empty partial, U never touched
       store_half_partial<D>(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, h, row < N, t_o, 0.f,
@@ -1052,26 +1095,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       } else if (o_fp32) {
         store_half_row<D>(o, lse, static_cast<size_t>(frow), h, row < N, true, t_o, l_row, m2, 1.f);
       } else {
-        // Row r of the staged tile: 128 bytes (64 bf16), 16-byte chunk c at chunk c ^ (r & 7)
-        // (the 128-byte swizzle of the O map); this thread's columns 32h .. 32h + 31 are chunks
-        // 4h .. 4h + 3.  Rows past N are staged too; the store does not write them.
-        uint32_t ur[32];
-        tmem_ld2_x32<32>(t_o, ur);
-        const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
-        if (h == 0 && row < N) lse[frow] = (l_row > 0.f) ? (m2 + log2f(l_row)) * kLn2 : -INFINITY;
+        // The staging is free (the previous store has read it); stage this thread's half row.
         ok = wait_all(BAR(C::B_OSF + t), gi & 1, abort_flag, budget);
         if (!ok) break;
-        const uint32_t srow = o_stage + static_cast<uint32_t>(r) * 128u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t* u = ur + 8 * i;
-          sts128(srow + ((static_cast<uint32_t>(4 * h + i) ^ static_cast<uint32_t>(r & 7)) << 4),
-                 pack_bf16(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
-                 pack_bf16(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
-                 pack_bf16(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
-                 pack_bf16(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
-        }
-        fence_proxy_async_smem();  // the TMA store reads the staging through the async proxy
+        stage_half_row<D>(o_stage, lse, static_cast<size_t>(frow), r, h, row < N, t_o, l_row, m2);
         mbar_arrive(BAR(C::B_OW + t));
         if (o_issuer) {
           ok = mbar_wait(BAR(C::B_OW + t), gi & 1, abort_flag, budget, &g_fwd_status);
@@ -1134,7 +1161,7 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
     if (aux.lin) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
     return launch_kernel(fwd_kernel<D, CAUSAL, FP8>, grid, C::THREADS, C::SMEM, stream, a.tq, a.tk, a.tv, a.o, a.lse,
-                         a.N, a.scale_log2, a.o_fp32, a.budget, aux);
+                         a.N, a.scale_log2, a.o_fp32, a.budget, aux, a.to);
   }
 }
 

@@ -210,6 +210,48 @@ __device__ __forceinline__ void store_half_partial(const FwdAux& aux, size_t slo
   }
 }
 
+// The new running row max, in exponent units (scores x c), from this thread's 64 scores of
+// the row (sr, raw fp32 bits; those from index `nvalid` on are masked to -inf in place) joined
+// with the other half of the row held by lane ^ 16.
+__device__ __forceinline__ float row_max_update(uint32_t (&sr)[64], int nvalid, float m2, float c) {
+  if (nvalid < 64) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
+  }
+  float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
+  float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
+#pragma unroll
+  for (int i = 4; i < 60; i += 8) {
+    a0 = fmax3(a0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+    a1 = fmax3(a1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+    a2 = fmax3(a2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+    a3 = fmax3(a3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+  }
+  a0 = fmax3(a0, __uint_as_float(sr[60]), __uint_as_float(sr[61]));
+  a1 = fmax3(a1, __uint_as_float(sr[62]), __uint_as_float(sr[63]));
+  float mx = fmax3(a0, a1, fmaxf(a2, a3));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // join the two halves of the row
+  return fmaxf(m2, mx * c);
+}
+
+// P~ = 2^(s c - m) of this thread's 64 scores as packed bf16 pairs, in place into sr[0..31]
+// (entry i holds keys 2i, 2i + 1 of the half row); their fp32 sum goes to rs_a + rs_b.
+__device__ __forceinline__ void exp_pack_bf16(uint32_t (&sr)[64], uint64_t c2, uint64_t nmb2, uint64_t& rs_a,
+                                              uint64_t& rs_b) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float x0, x1, x2, x3;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0, x1);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2, x3);
+    const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+    rs_a = f2_add(rs_a, f2_pack(p0, p1));
+    rs_b = f2_add(rs_b, f2_pack(p2, p3));
+    sr[i] = pack_bf16(p0, p1);
+    sr[i + 1] = pack_bf16(p2, p3);
+  }
+}
+
 // This thread's half of an O row = U / l as bf16 into a staged O tile for the TMA store, and
 // lse from the h = 0 thread.  The tile is D/64 boxes of 128 rows x 128 bytes with the 128-byte
 // swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); the thread's D/2 columns are chunks
@@ -573,26 +615,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(BAR(C::B_SC + t));  // S_t(j) is in registers: the MMA may overwrite it
       }
-      const int nvalid = lim - j * kBc - 64 * h + 1;  // admissible keys among them
-      if (nvalid < 64) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
-      }
-      float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
-      float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
-#pragma unroll
-      for (int i = 4; i < 60; i += 8) {
-        a0 = fmax3(a0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-        a1 = fmax3(a1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-        a2 = fmax3(a2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-        a3 = fmax3(a3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
-      }
-      a0 = fmax3(a0, __uint_as_float(sr[60]), __uint_as_float(sr[61]));
-      a1 = fmax3(a1, __uint_as_float(sr[62]), __uint_as_float(sr[63]));
-      float mx = fmax3(a0, a1, fmaxf(a2, a3));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // join the two halves of the row
-      const float m_new = fmaxf(m2, mx * cj);
+      // admissible keys among this thread's 64 columns
+      const float m_new = row_max_update(sr, lim - j * kBc - 64 * h + 1, m2, cj);
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
       const float alpha = ex2(m2 - mb);
       const uint64_t nmb2 = f2_pack(-mb, -mb);
@@ -620,20 +644,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
             sr[i] = pack_e4m3x4(p0, p1, p2, p3);
           }
         } else {
-          // P~ packed in place into sr[0..31] (entry i holds keys 64h + 2i, 2i + 1).
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1, x2, x3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0,
-                      x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2,
-                      x3);
-            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-            rs_a = f2_add(rs_a, f2_pack(p0, p1));
-            rs_b = f2_add(rs_b, f2_pack(p2, p3));
-            sr[i] = pack_bf16(p0, p1);
-            sr[i + 1] = pack_bf16(p2, p3);
-          }
+          exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);  // P~ packed in place into sr[0..31]
         }
         // PV_t(j-1) must be done before P~_t(j) overwrites P~_t(j-1) and before U_t is rescaled.
         if (j > 0) {
@@ -1019,43 +1030,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
         tc_fence_before();
         mbar_arrive(BAR(C::B_SC + t));  // S_t(j) is in registers: the MMA may overwrite it
-        const int nvalid = lim - j * kBc - 64 * h + 1;  // keys of the item among them
-        if (nvalid < 64) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
-        }
-        float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
-        float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
-#pragma unroll
-        for (int i = 4; i < 60; i += 8) {
-          a0 = fmax3(a0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-          a1 = fmax3(a1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-          a2 = fmax3(a2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-          a3 = fmax3(a3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
-        }
-        a0 = fmax3(a0, __uint_as_float(sr[60]), __uint_as_float(sr[61]));
-        a1 = fmax3(a1, __uint_as_float(sr[62]), __uint_as_float(sr[63]));
-        float mx = fmax3(a0, a1, fmaxf(a2, a3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // join the two halves of the row
-        const float m_new = fmaxf(m2, mx * sl2);
+        // keys of the item among this thread's 64 columns
+        const float m_new = row_max_update(sr, lim - j * kBc - 64 * h + 1, m2, sl2);
         const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
         const float alpha = ex2(m2 - mb);
         const uint64_t nmb2 = f2_pack(-mb, -mb);
         uint64_t rs_a = f2_pack(0.f, 0.f), rs_b = rs_a;
-        // P~ packed in place into sr[0..31] (entry i holds keys 64h + 2i, 2i + 1).
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nmb2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i + 2]), __uint_as_float(sr[2 * i + 3])), c2, nmb2), x2,
-                    x3);
-          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          rs_a = f2_add(rs_a, f2_pack(p0, p1));
-          rs_b = f2_add(rs_b, f2_pack(p2, p3));
-          sr[i] = pack_bf16(p0, p1);
-          sr[i + 1] = pack_bf16(p2, p3);
-        }
+        exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);  // P~ packed in place into sr[0..31]
         // PV_t(j-1) must be done before P~_t(j) overwrites P~_t(j-1) and before U_t is rescaled
         // (for j = 0 the previous item's epilogue waited for its last PV).
         if (j > 0) {

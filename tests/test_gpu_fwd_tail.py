@@ -67,8 +67,18 @@ def test_tail_split_small_all_rows(B, H, N, d, o_fp32):
     assert float((lse - l1).abs().max()) <= 1e-4
 
 
+def test_tail_split_prefill_workload_all_rows():
+    # the bench's launch: B4 H16 N2048 d64 with bf16 O, 512 blocks on 152 SMs, the last 56 cut
+    # into two key halves; every row against the oracle
+    w = inputs.WORKLOADS["prefill"]
+    q, k, v = inputs.workload_inputs(w, seed=0, device=DEV)
+    o, lse = run_tail(q, k, v, w.scale, False)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, False)
+    assert_parity(o, lse, o_ref, lse_ref, "prefill tail, all rows (bf16 O)")
+
+
 def test_tail_split_prefill_workload():
-    # B4 H16 N2048 d64: 512 blocks on 152 SMs, the last 56 cut into two key halves
+    # the same launch with fp32 O and bf16 O on sampled rows (and tile edges)
     w = inputs.WORKLOADS["prefill"]
     q, k, v = inputs.workload_inputs(w, seed=0, device=DEV)
     rows = inputs.sample_rows_per_head(w.B, w.H, w.N, 96, seed=8)

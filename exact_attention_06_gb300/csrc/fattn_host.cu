@@ -421,6 +421,7 @@ fa_status_t fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const flo
   if ((st = make_map(&a.tq, q8, d, N, bh, 128, 1)) != FA_OK) return st;
   if ((st = make_map(&a.tk, k8, d, N, bh, 128, 1)) != FA_OK) return st;
   if ((st = make_map(&a.tv, v8, d, N, bh, 128, 1)) != FA_OK) return st;
+  if (!o_fp32 && (st = make_map(&a.to, o, d, N, bh, 128)) != FA_OK) return st;
   a.o = o;
   a.lse = lse;
   a.N = N;

@@ -24,6 +24,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "stage_io.cuh"
 #include "tmem_io.cuh"
 
 namespace fattn {
@@ -219,7 +220,8 @@ struct DkdvCfg : BwdCfg<D> {
   static constexpr uint32_t OFF_VEC = OFF_RING + B::ST * STAGE;
   static constexpr uint32_t OFF_BAR = OFF_VEC + B::ST * B::VEC;
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
-                       B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;  // B_PF + c: chunk c of the elementwise step
+                       B_DRAIN = B_PF + 2, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;  // B_PF + c: chunk c of the
+                                                                               // elementwise step
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
 };
@@ -231,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dk,
                     void* __restrict__ dv, int N, float sl2, float scale, int grad_fp32,
-                    unsigned long long budget) {
+                    unsigned long long budget, const __grid_constant__ CUtensorMap tdk,
+                    const __grid_constant__ CUtensorMap tdv) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::B_PF), kEwWarps * 32);
     mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
     mbar_init(BAR(C::B_DRAIN), 1);
+    mbar_init(BAR(C::B_OW), kEwWarps * 32);  // bf16 gradients staged
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -399,8 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const size_t row_off = static_cast<size_t>(bh) * N + key;
-      store_grad_half_row<D>(dv, row_off, h, key < N, grad_fp32 != 0, tmem + lane_addr + kColG1, 1.f);
-      store_grad_half_row<D>(dk, row_off, h, key < N, grad_fp32 != 0, tmem + lane_addr + C::COL_G2, scale);
+      if (grad_fp32) {
+        store_grad_half_row<D>(dv, row_off, h, key < N, true, tmem + lane_addr + kColG1, 1.f);
+        store_grad_half_row<D>(dk, row_off, h, key < N, true, tmem + lane_addr + C::COL_G2, scale);
+      } else {
+        // bf16 dV and dK through shared memory: the V and K tiles have their shape and are no
+        // longer read (every product MMA is complete); one thread stores them with TMA.
+        stage_half_row_bf16<D>(sV, sV + kBox, r, h, tmem + lane_addr + kColG1, 1.f);
+        stage_half_row_bf16<D>(sK, sK + kBox, r, h, tmem + lane_addr + C::COL_G2, scale);
+        mbar_arrive(BAR(C::B_OW));
+        if (warp == 0 && lane == 0 && bwait(BAR(C::B_OW), 0, abort_flag, budget)) {
+          for (int hb = 0; hb < C::NH; ++hb) {
+            tma_store_3d(&tdv, sV + static_cast<uint32_t>(hb) * kBox, hb * 64, kt * kTile, bh);
+            tma_store_3d(&tdk, sK + static_cast<uint32_t>(hb) * kBox, hb * 64, kt * kTile, bh);
+          }
+          bulk_commit();
+          bulk_wait_all();  // complete before the CTA exits
+        }
+      }
     }
     tmem_wait_st();
   }
@@ -423,7 +443,8 @@ struct DqCfg : BwdCfg<D> {
   static constexpr uint32_t STAGE = 2 * B::TB;
   static constexpr uint32_t OFF_BAR = OFF_RING + B::ST * STAGE;
   static constexpr int B_QD = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
-                       B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;  // B_PF + c: chunk c of the elementwise step
+                       B_DRAIN = B_PF + 2, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;  // B_PF + c: chunk c of the
+                                                                               // elementwise step
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
 };
@@ -434,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dq, int N,
-                  float sl2, float scale, int grad_fp32, unsigned long long budget) {
+                  float sl2, float scale, int grad_fp32, unsigned long long budget,
+                  const __grid_constant__ CUtensorMap tdq) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -461,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::B_PF), kEwWarps * 32);
     mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
     mbar_init(BAR(C::B_DRAIN), 1);
+    mbar_init(BAR(C::B_OW), kEwWarps * 32);  // bf16 gradients staged
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -581,8 +604,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = bwait_all(BAR(C::B_SF), n_j & 1, abort_flag, budget);
     if (ok) {
       tc_fence_after();
-      store_grad_half_row<D>(dq, static_cast<size_t>(bh) * N + row, h, in, grad_fp32 != 0, tmem + lane_addr + kColG1,
-                             scale);
+      if (grad_fp32) {
+        store_grad_half_row<D>(dq, static_cast<size_t>(bh) * N + row, h, in, true, tmem + lane_addr + kColG1, scale);
+      } else {
+        // bf16 dQ through shared memory: the Q tile has its shape and is no longer read
+        stage_half_row_bf16<D>(sQ, sQ + kBox, r, h, tmem + lane_addr + kColG1, scale);
+        mbar_arrive(BAR(C::B_OW));
+        if (warp == 0 && lane == 0 && bwait(BAR(C::B_OW), 0, abort_flag, budget)) {
+          for (int hb = 0; hb < C::NH; ++hb)
+            tma_store_3d(&tdq, sQ + static_cast<uint32_t>(hb) * kBox, hb * 64, qt * kTile, bh);
+          bulk_commit();
+          bulk_wait_all();  // complete before the CTA exits
+        }
+      }
     }
     tmem_wait_st();
   }
@@ -609,13 +643,13 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
   if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM)) != cudaSuccess)
     return e;
   k1<<<grid, kThreads, DkdvCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dk, a.dv, a.N,
-                                                   a.scale_log2, a.scale, a.grad_fp32, a.budget);
+                                                   a.scale_log2, a.scale, a.grad_fp32, a.budget, a.tdk, a.tdv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto k2 = bwd_dq_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM)) != cudaSuccess)
     return e;
   k2<<<grid, kThreads, DqCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dq, a.N, a.scale_log2,
-                                                 a.scale, a.grad_fp32, a.budget);
+                                                 a.scale, a.grad_fp32, a.budget, a.tdq);
   return cudaGetLastError();
 }
 

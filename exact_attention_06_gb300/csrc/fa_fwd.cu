@@ -55,6 +55,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "stage_io.cuh"
 #include "tmem_io.cuh"
 
 namespace fattn {
@@ -252,31 +253,9 @@ __device__ __forceinline__ void exp_pack_bf16(uint32_t (&sr)[64], uint64_t c2, u
   }
 }
 
-// This thread's half of an O row = o_mult * U / l as bf16 into a staged O tile for the TMA
-// store, and lse from the h = 0 thread.  The tile is D/64 boxes (at box0, box1) of 128 rows x
-// 128 bytes with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); the
-// thread's D/2 columns are chunks 4h .. 4h + 3 of the one box at D = 64 and all 8 chunks of box
-// h at D = 128.  Every lane runs the TMEM load (it is warp-collective); rows past N are staged
-// too (the store skips them).
-template <int D>
-__device__ __forceinline__ void stage_half_row(uint32_t box0, uint32_t box1, float* lse, size_t row_off, int r,
-                                               int h, bool valid, uint32_t taddr, float l, float m2, float o_mult) {
-  uint32_t ur[D / 2];
-  if constexpr (D == 128) tmem_ld2_x64<64>(taddr, ur); else tmem_ld2_x32<32>(taddr, ur);
-  const float inv = (l > 0.f) ? o_mult / l : 0.f;
+// lse of this thread's row from the h = 0 thread, rows < N only.
+__device__ __forceinline__ void store_lse(float* lse, size_t row_off, int h, bool valid, float l, float m2) {
   if (h == 0 && valid) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
-  const uint32_t srow = (D == 128 && h ? box1 : box0) + static_cast<uint32_t>(r) * 128u;
-  const int c0 = D == 128 ? 0 : 4 * h;
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i) {
-    const uint32_t* u = ur + 8 * i;
-    sts128(srow + ((static_cast<uint32_t>(c0 + i) ^ static_cast<uint32_t>(r & 7)) << 4),
-           pack_bf16(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
-           pack_bf16(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
-           pack_bf16(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
-           pack_bf16(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
-  }
-  fence_proxy_async_smem();  // the TMA store reads the staging through the async proxy
 }
 
 template <int D, bool CAUSAL, bool FP8>
@@ -716,8 +695,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         // thread stores it with TMA once all 256 threads have written.
         const uint32_t box0 = sQ + static_cast<uint32_t>(t) * C::QB;
         const uint32_t box1 = FP8 ? base + C::OFF_P + static_cast<uint32_t>(t) * C::PB : box0 + kBox;
-        stage_half_row<D>(box0, box1, lse, static_cast<size_t>(bh) * N + row, r, h, row < N, t_o, l_row, m2,
-                          FP8 ? sv_max * (1.f / 256.f) : 1.f);
+        store_lse(lse, static_cast<size_t>(bh) * N + row, h, row < N, l_row, m2);
+        stage_half_row_bf16<D>(box0, box1, r, h, t_o, (l_row > 0.f) ? (FP8 ? sv_max * (1.f / 256.f) : 1.f) / l_row : 0.f);
         mbar_arrive(BAR(C::B_OW + t));
         if ((warp % kSoftmaxWarps) == 0 && lane == 0 &&
             mbar_wait(BAR(C::B_OW + t), 0, abort_flag, budget, &g_fwd_status)) {
@@ -1084,7 +1063,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // The staging is free (the previous store has read it); stage this thread's half row.
         ok = wait_all(BAR(C::B_OSF + t), gi & 1, abort_flag, budget);
         if (!ok) break;
-        stage_half_row<D>(o_stage, o_stage, lse, static_cast<size_t>(frow), r, h, row < N, t_o, l_row, m2, 1.f);
+        store_lse(lse, static_cast<size_t>(frow), h, row < N, l_row, m2);
+        stage_half_row_bf16<D>(o_stage, o_stage, r, h, t_o, (l_row > 0.f) ? 1.f / l_row : 0.f);
         mbar_arrive(BAR(C::B_OW + t));
         if (o_issuer) {
           ok = mbar_wait(BAR(C::B_OW + t), gi & 1, abort_flag, budget, &g_fwd_status);

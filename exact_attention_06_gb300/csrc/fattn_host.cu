@@ -662,6 +662,11 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   if ((st = make_map(&a.tk, k, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tv, v, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tdo, dout, d, N, bh, 128)) != FA_OK) return st;
+  if (!grad_fp32) {
+    if ((st = make_map(&a.tdq, dq, d, N, bh, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tdk, dk, d, N, bh, 128)) != FA_OK) return st;
+    if ((st = make_map(&a.tdv, dv, d, N, bh, 128)) != FA_OK) return st;
+  }
   a.o = o;
   a.dout = dout;
   a.lse = lse;

@@ -95,6 +95,7 @@ unsigned int decode_read_and_clear_status();
 // 64 x 128 boxes and 128-byte swizzle; delta is the caller's [B*H, N] fp32 scratch.
 struct BwdLaunch {
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tdq, tdk, tdv;  // bf16 gradients as {d, N, B*H} for the TMA stores (unused for fp32)
   const void* o;
   const void* dout;
   const float* lse;

@@ -4,10 +4,10 @@
 
 One JSON line on rank 0.  The headline workload is the prefill configuration
 (B=4, H=16, N=2048, d=64, non-causal, bf16): one step is one fa_fwd_ex call over
-it (the fused forward; its 512 blocks of 256 query rows fill 3.37 waves of the
-152 SMs, so the last wave's blocks are split along the keys and a combine kernel
-merges them), timed with CUDA events on the launching stream, L2 flushed
-(256 MiB write) between timed steps because its inputs (50 MB) fit in L2.
+it (the persistent fused forward; its 512 blocks of 256 query rows fill 3.37
+rounds of the 152 SMs, so the last round's 56 blocks run as 112 single query
+tiles), timed with CUDA events on the launching stream, L2 flushed (256 MiB
+write) between timed steps because its inputs (50 MB) fit in L2.
 ``extra`` carries the other workloads of the target (causal N=8192 d=128 with
 x8 key spikes, ragged causal N=16381, split-KV decode L=32768) and of the
 library's further paths (backward and FP8 forward on the causal workload, the
@@ -195,8 +195,8 @@ def _prefill_step_fn(w, dev, stream):
 
 
 def _tail_workspace(w, dev):
-    """The forward's tail-split workspace for this workload on this device (None: no split
-    planned, one launch; otherwise the forward and the combine of the split blocks)."""
+    """The workspace of the forward's key split for this workload on this device (None: no key
+    split planned, one launch; otherwise the forward and the combine of the split blocks)."""
     import torch
     from exact_attention_06_gb300 import fattn
     nbytes = fattn.fa_fwd_workspace_bytes(w.B, w.H, w.N, w.d, w.causal)
@@ -563,8 +563,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}", "l2": "flushed between timed steps (256 MiB write)"},
         "gpu_launches": launches * args.steps,
         "roofline": dict(_roofline("tensor", flops, t_local, peaks, _traffic("fwd_persist_kernel", HEADLINE)),
-                         note="duration covers the forward kernel and, when the tail is split, the combine "
-                              "kernel; traffic is the forward kernel's"),
+                         note="duration covers the step's launches (the forward kernel, and the combine when "
+                              "the last round is split by keys); traffic is the forward kernel's"),
         "clocks": sampler.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -729,8 +729,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 // Persistent forward for non-causal bf16 at d = 64: one CTA per SM walks its work items
 // (blockIdx.x, + gridDim.x, ...).  An item is a block of 256 query rows (two tiles) of one (b, h)
 // against the keys koff .. koff + Nk - 1, loaded from key row kload; the blocks run in
-// (b*h, block) order, and with the tail split (aux.lin) the blocks from n_full on are cut into
-// ksplit key pieces that leave partial (U, m, l) rows for the combine kernel.  Between items a
+// (b*h, block) order.  The blocks from n_full on (a partly filled last round) may be cut: into
+// ksplit key pieces that leave partial (U, m, l) rows for the combine kernel (aux.lin, the tail
+// split), or into their two query tiles, each an item of its own (aux.qsplit).  Between items a
 // CTA keeps its TMEM, barriers and K/V ring: the next Q is loaded as soon as the last S MMAs of
 // the current item have read Q, and the next item's S(0) is issued right after the current
 // item's last PV, under the softmax warps' epilogue.  The step itself is the separate-P~
@@ -752,7 +753,11 @@ __device__ __forceinline__ FwdItem item_at(int w, const FwdAux& aux, int N) {
   I.smul = aux.S;
   I.sadd = aux.shard;
   const int n_pairs = (N + kRowsPerCta - 1) / kRowsPerCta;
-  int u = w;
+  int u = w, tile = -1;  // tile: the one query tile of a query-split item (-1: both)
+  if (aux.qsplit && w >= aux.n_full) {
+    u = aux.n_full + (w - aux.n_full) / 2;
+    tile = (w - aux.n_full) % 2;
+  }
   if (aux.lin && w >= aux.n_full) {
     const int piece = w - aux.n_full;
     u = aux.n_full + piece / aux.ksplit;
@@ -766,8 +771,8 @@ __device__ __forceinline__ FwdItem item_at(int w, const FwdAux& aux, int N) {
   I.bh = u / n_pairs;
   I.pair = u % n_pairs;
   const int n_tiles = (I.Nk + kBc - 1) / kBc;
-  I.n0 = n_tiles;  // tile 0 of a block is inside N
-  I.n1 = I.pair * kRowsPerCta + kBr < N ? n_tiles : 0;
+  I.n0 = tile == 1 ? 0 : n_tiles;  // tile 0 of a block is inside N; a query-split item runs one of the two
+  I.n1 = (tile != 0 && I.pair * kRowsPerCta + kBr < N) ? n_tiles : 0;
   return I;
 }
 
@@ -843,7 +848,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       bool ok = true;
       for (int w = w0, it = 0; ok && w < n_items; w += w_step, ++it) {
         const FwdItem I = item_at(w, aux, N);
-        const int n_max = I.n0;
+        const int n_max = max(I.n0, I.n1);
         // The previous item's Q is free once both tiles' last S MMAs have completed.
         if (it > 0 && !mbar_wait(BAR(C::B_QE), (it - 1) & 1, abort_flag, budget, &g_fwd_status)) break;
         mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QB);
@@ -922,7 +927,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       bool ok = true, issued = false;
       for (int w = w0, it = 0; ok && w < n_items; w += w_step, ++it) {
         const FwdItem I = item_at(w, aux, N);
-        const int n = t ? I.n1 : I.n0, n_max = I.n0;
+        const int n = t ? I.n1 : I.n0, n_max = max(I.n0, I.n1);
         // This item's Q (waited for first in every case, so that this warp's release of Q below
         // falls into this item's phase).
         ok = wait(BAR(C::B_Q), it & 1);
@@ -1116,7 +1121,9 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
   if constexpr (!CAUSAL && !FP8 && D == 64) {
     // the persistent kernel: one CTA per SM over the work items
     const long long units = static_cast<long long>(a.BH) * n_pairs;
-    const long long items = aux.lin ? aux.n_full + (units - aux.n_full) * aux.ksplit : units;
+    const long long items = aux.lin      ? aux.n_full + (units - aux.n_full) * aux.ksplit
+                            : aux.qsplit ? aux.n_full + (units - aux.n_full) * 2
+                                         : units;
     if (items > INT_MAX) return cudaErrorInvalidValue;
     aux.n_items = static_cast<int>(items);
     const dim3 grid(static_cast<unsigned>(a.sms > 0 ? std::min<long long>(items, a.sms) : items));

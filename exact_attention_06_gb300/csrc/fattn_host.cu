@@ -171,14 +171,19 @@ fa_status_t plan_paged(int B, int H, int L, int d, int page_size, int splits, in
   return plan_decode(B, H, L, d, 128, (n_chunks + chunks_per_split - 1) / chunks_per_split, 0, plan);
 }
 
-// Tail split of the non-causal d = 64 forward.  With one resident CTA per SM, U blocks of 256 query
-// rows run in ceil(U / sms) waves, the last holding rem blocks.  Cutting each of those rem blocks
-// into k key pieces (>= 2 key tiles each) spreads the last wave over k * rem CTAs, whose partial
-// (U, m, l) rows the combine kernel then merges.  Costs are counted in key-tile steps: a CTA's
-// prologue and epilogue about 2 steps, the combine about 1.5.  A split is taken when it saves at
-// least 5 % of the whole launch.
+// The last round of the non-causal d = 64 forward.  With one resident CTA per SM, U blocks of 256
+// query rows run in ceil(U / sms) rounds, the last holding rem blocks.  Two ways to spread that
+// round over more SMs:
+//   key split: each of the rem blocks becomes k key pieces (>= 2 key tiles each) that leave
+//     partial (U, m, l) rows, merged by the combine kernel (needs a workspace);
+//   query split: each becomes two single-tile items (when 2 * rem <= sms; no workspace).
+// Costs are counted in key-tile steps of a whole block: a block costs its n key tiles plus ~2
+// of set-up and epilogue, a piece its share plus 2, the combine (with its launch) ~3; a
+// single-tile item runs alone on its SM at ~0.72 of a whole block (both measured on GB300).
+// The cheapest wins if it saves at least 5 % of the launch; ties go to the query split.
 struct TailPlan {
-  int ksplit = 1;  // 1: no split
+  int ksplit = 1;  // > 1: key split into ksplit pieces
+  int qsplit = 0;  // 1: query split (used when there is no key split, with or without a workspace)
   int n_full = 0, kchunk = 0;
   long long prow0 = 0, rows = 0;
   size_t u_bytes = 0, m_bytes = 0, l_bytes = 0;
@@ -187,14 +192,15 @@ struct TailPlan {
 
 TailPlan plan_tail(long long bh, int N, int d, int causal, int sms) {
   TailPlan p;
-  if (causal || d != 64 || sms < 1) return p;  // the persistent d = 64 kernel runs the pieces
+  if (causal || d != 64 || sms < 1) return p;  // the persistent d = 64 kernel runs the split rounds
   const long long n_pairs = (N + 255) / 256;
   const long long U = bh * n_pairs;
   const int n_tiles = (N + 127) / 128;
   const long long waves = (U + sms - 1) / sms;
   const long long rem = U - (waves - 1) * sms;
-  constexpr double kFixed = 2.0, kCombine = 1.5;
+  constexpr double kFixed = 2.0, kCombine = 3.0, kSingleTile = 0.72;
   const double t_whole = n_tiles + kFixed;
+  const double t_q = 2 * rem <= sms ? kSingleTile * t_whole : t_whole;
   double best_t = t_whole;
   int best_k = 1, best_tpp = n_tiles;
   for (int k = 2; k <= 8 && 2 * k <= n_tiles; ++k) {
@@ -207,11 +213,13 @@ TailPlan plan_tail(long long bh, int N, int d, int causal, int sms) {
       best_tpp = tpp;
     }
   }
-  if (best_k == 1 || t_whole - best_t < 0.05 * waves * t_whole) return p;
-  if (U - rem + rem * best_k > INT_MAX) return p;
+  const double margin = 0.05 * waves * t_whole;
+  if (U - rem + 2 * rem > INT_MAX || U - rem + rem * best_k > INT_MAX) return p;
+  p.n_full = static_cast<int>(U - rem);
+  if (t_q < t_whole - margin) p.qsplit = 1;  // the fallback whenever there is no key split
+  if (best_k == 1 || best_t >= t_q || t_whole - best_t < margin) return p;
   p.ksplit = best_k;
   p.kchunk = best_tpp * 128;
-  p.n_full = static_cast<int>(U - rem);
   p.prow0 = (p.n_full / n_pairs) * N + (p.n_full % n_pairs) * 256;
   p.rows = bh * N - p.prow0;
   p.u_bytes = round256(static_cast<size_t>(p.rows) * best_k * d * sizeof(float));
@@ -274,7 +282,8 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   fa_status_t st = check_device(&sms);
   if (st != FA_OK) return st;
   void* ws = opts ? opts->workspace : nullptr;
-  const TailPlan tail = ws ? plan_tail(bh, N, d, causal, sms) : TailPlan{};
+  TailPlan tail = plan_tail(bh, N, d, causal, sms);
+  if (!ws) tail.ksplit = 1;  // no workspace: no key split (the query split still applies)
   if (tail.ksplit > 1) {
     if (opts->workspace_bytes < tail.total())
       return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes fa_fwd_workspace_bytes gives",
@@ -298,6 +307,10 @@ fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
   a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
   a.aux.Nk = N;
   a.sms = sms;
+  if (tail.ksplit == 1 && tail.qsplit) {  // the last round's blocks as single query tiles
+    a.aux.qsplit = 1;
+    a.aux.n_full = tail.n_full;
+  }
   if (tail.ksplit > 1) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     a.aux.lin = 1;

@@ -38,6 +38,9 @@ struct FwdAux {
   int ksplit;
   int kchunk;
   long long prow0;
+  // Query split (persistent kernel, lin = 0): the blocks from n_full on run as two single-tile
+  // items each (items n_full + 2*(block - n_full) + tile).
+  int qsplit;
   // Persistent CTAs (non-causal bf16): the number of work items; set by launch_fwd.
   int n_items;
 };

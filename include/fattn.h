@@ -86,25 +86,27 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
 /* fa_fwd with options (opts may be NULL).  With opts->o_fp32 = 1, `o` is an
  * fp32 [B, H, N, d] tensor.
  *
- * Tail split (non-causal, d = 64): the forward works on blocks of 256 query
- * rows of a (b, h), one block per SM at a time, so when the last round of
- * blocks only partly fills the SMs most of them idle through it.  Given a
- * workspace of fa_fwd_workspace_bytes() bytes, the blocks of that last round
- * are instead split along the keys into pieces
- * that each leave a partial (U, m, l) per row, and a second kernel merges them
- * by the online-softmax rule, as the split-KV decode does (FlashDecoding
- * split-K, cnblogs jzssuanfa page, §三 场景 B).  O and lse are the same
- * function of q, k, v up to rounding order.  With a workspace too small for
- * the plan: FA_ERR_WORKSPACE. */
+ * The last round (non-causal, d = 64): the forward works on blocks of 256
+ * query rows of a (b, h), one block per SM at a time, so when the last round
+ * of blocks only partly fills the SMs most of them idle through it.  Such a
+ * round is split, whichever of two ways the plan (by the device's SM count)
+ * finds cheaper: its blocks run as their two 128-row query tiles, each on an
+ * SM of its own (no workspace); or, given a workspace of
+ * fa_fwd_workspace_bytes() bytes, they are cut along the keys into pieces that
+ * each leave a partial (U, m, l) per row, which a second kernel merges by the
+ * online-softmax rule, as the split-KV decode does (FlashDecoding split-K,
+ * cnblogs jzssuanfa page, §三 场景 B).  O and lse are the same function of
+ * q, k, v up to rounding order.  With a workspace too small for the plan:
+ * FA_ERR_WORKSPACE. */
 fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                       int B, int H, int N, int d, float scale, int causal, void* stream,
                       const fa_fwd_opts* opts);
 
-/* fa_fwd_workspace_bytes -- scratch bytes the tail split of fa_fwd_ex needs on
- * the current device for this problem, or 0 when it plans no split (causal
- * launches, d = 128, last waves that are nearly full, fewer than 4 key tiles,
- * invalid sizes, no sm_103a device).  The plan depends on the device's SM
- * count. */
+/* fa_fwd_workspace_bytes -- scratch bytes the key split of fa_fwd_ex's last
+ * round needs on the current device for this problem, or 0 when it plans no
+ * key split (causal launches, d = 128, last rounds that are nearly full or
+ * that the query split serves as well, fewer than 4 key tiles, invalid sizes,
+ * no sm_103a device).  The plan depends on the device's SM count. */
 size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal);
 
 /*

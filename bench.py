@@ -63,15 +63,15 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 51.459e6,
-                                        "sha256": "7105aea4e874ed256a8c563c16c9bb10407761f6d653a44daa8aaf95f37a6717"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 587.747e6,
-                               "sha256": "7105aea4e874ed256a8c563c16c9bb10407761f6d653a44daa8aaf95f37a6717"},
-    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 215.682e6,
-                                   "sha256": "7105aea4e874ed256a8c563c16c9bb10407761f6d653a44daa8aaf95f37a6717"},
+    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 50.783e6,
+                                        "sha256": "3109548895bd2578c65db6172e2be5590eac535cf1e2cd1a98a8f37ed1acbb10"},
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 594.590e6,
+                               "sha256": "3109548895bd2578c65db6172e2be5590eac535cf1e2cd1a98a8f37ed1acbb10"},
+    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 227.113e6,
+                                   "sha256": "3109548895bd2578c65db6172e2be5590eac535cf1e2cd1a98a8f37ed1acbb10"},
     # backward: the dominant kernel (dK/dV) on the causal workload
-    ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1047.634e6,
-                                    "sha256": "208eadff17955d1b0a7ede7c25dee933060383e41355730a0af1970b6029767a"},
+    ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1060.249e6,
+                                    "sha256": "989af07c8d9f2cef598efdd2625961591aac3471fb8465e545ad689f6f41316b"},
     # decode: captured on the B4 slice (decode_small) and scaled by 16 to B64 (K/V streamed once)
     ("decode_split_kernel", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2151.001e6,
                                         "sha256": "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"},

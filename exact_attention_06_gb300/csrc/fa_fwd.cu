@@ -649,23 +649,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           tmem_st2_x32<32>(t_p, pr);
         }
       }
+      if constexpr (!C::SEP) {
+        // P~ packed in place into sr[0..31], then this thread's 32 packed columns (32h ..) of S_t
+        exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);
+        uint32_t pr[32];
 #pragma unroll
-      for (int q = 0; q < (C::SEP ? 0 : 2); ++q) {
-        uint32_t pr[16];
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const int e = 32 * q + 2 * i;
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2), x2, x3);
-          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          rs_a = f2_add(rs_a, f2_pack(p0, p1));
-          rs_b = f2_add(rs_b, f2_pack(p2, p3));
-          pr[i] = pack_bf16(p0, p1);
-          pr[i + 1] = pack_bf16(p2, p3);
-        }
-        // P~ keys 64h + 32q .. +31 -> packed columns 32h + 16q .. +15
-        tmem_st2_x16<32>(t_s + 16 * q, pr);
+        for (int i = 0; i < 32; ++i) pr[i] = sr[i];
+        tmem_st2_x32<32>(t_s, pr);
       }
       float s0, s1, s2, s3;
       f2_unpack(rs_a, s0, s1);

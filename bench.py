@@ -63,12 +63,12 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 50.783e6,
-                                        "sha256": "3109548895bd2578c65db6172e2be5590eac535cf1e2cd1a98a8f37ed1acbb10"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 594.590e6,
-                               "sha256": "3109548895bd2578c65db6172e2be5590eac535cf1e2cd1a98a8f37ed1acbb10"},
-    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 227.113e6,
-                                   "sha256": "3109548895bd2578c65db6172e2be5590eac535cf1e2cd1a98a8f37ed1acbb10"},
+    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 50.806e6,
+                                        "sha256": "8ce9ad5fd573ae9ad5bde635e7bd1a79c3b5a1621a130322717c60d010a367ce"},
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 592.465e6,
+                               "sha256": "8ce9ad5fd573ae9ad5bde635e7bd1a79c3b5a1621a130322717c60d010a367ce"},
+    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 228.017e6,
+                                   "sha256": "8ce9ad5fd573ae9ad5bde635e7bd1a79c3b5a1621a130322717c60d010a367ce"},
     # backward: the dominant kernel (dK/dV) on the causal workload
     ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1060.249e6,
                                     "sha256": "989af07c8d9f2cef598efdd2625961591aac3471fb8465e545ad689f6f41316b"},

@@ -85,3 +85,42 @@ def test_forward_wide_grid():
         assert_parity(got_o, got_l, o_ref, lse_ref, f"b{b} h{h}")
     # and no row anywhere is left unwritten
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_back_to_back_dependent_launches(d, causal):
+    # The forward is launched with programmatic stream serialization: its set-up may overlap the
+    # previous kernel, and its global accesses must wait for it.  Chain three forwards on one
+    # stream without a synchronisation, each reading the previous one's output as its q (and
+    # writing over the buffer the previous one read), then check every link against the oracle.
+    B, H, N = 1, 4, 700
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=40 + d, device=DEV)
+    bufs = [q.clone(), torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)]
+    lses = [torch.empty((B, H, N), dtype=torch.float32, device=DEV) for _ in range(3)]
+    for i in range(3):
+        fattn.fa_fwd_ex(bufs[i], k, v, bufs[i + 1], lses[i], scale, causal)
+    fattn.fa_get_status()
+    for i in range(3):
+        o_ref, lse_ref = oracle.attention(bufs[i].cpu(), k.cpu(), v.cpu(), scale, causal)
+        assert_parity(bufs[i + 1], lses[i], o_ref, lse_ref, f"link {i}")
+
+
+def test_back_to_back_ping_pong_overwrites_inputs():
+    # Two buffers A, B: A -> B, B -> A, A -> B.  The second launch overwrites A while the first
+    # one reads it unless its writes wait for the first launch to complete.  The oracle chains
+    # the same three steps, rounding each output to bf16 as the next input.
+    B, H, N, d = 1, 4, 700, 64
+    scale = 0.125
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=50, device=DEV)
+    a, b = q.clone(), torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    fattn.fa_fwd_ex(a, k, v, b, lse, scale, False)
+    fattn.fa_fwd_ex(b, k, v, a, lse, scale, False)
+    fattn.fa_fwd_ex(a, k, v, b, lse, scale, False)
+    fattn.fa_get_status()
+    x = q.cpu()
+    for _ in range(3):
+        o_ref, lse_ref = oracle.attention(x, k.cpu(), v.cpu(), scale, False)
+        x = torch.from_numpy(o_ref).reshape(B, H, N, d).to(torch.bfloat16)
+    assert_parity(b, lse, o_ref, lse_ref, "ping-pong")

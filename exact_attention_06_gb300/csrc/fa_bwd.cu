@@ -160,6 +160,24 @@ __device__ __forceinline__ void issue_grad_part(uint32_t d_tmem, uint32_t a_tmem
   }
 }
 
+// G (+)= X_q Y_q for query half q of the dK/dV kernel: X_q is the packed bf16 half of the 128 x
+// 128 TMEM tile (columns 64q .. 64q + 63; the thread holding queries 64q + 32h .. writes them
+// packed at columns 64q + 32h .. + 15, so K block 4q + m, m < 2 from h = 0 and m >= 2 from
+// h = 1, is at column 64q + 32(m / 2) + 8(m % 2)), Y_q rows 64q .. 64q + 63 of a 128 x d MN-major
+// tile.  Four MMAs of 16 queries each.
+template <int D>
+__device__ __forceinline__ void issue_grad_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idesc,
+                                                bool accumulate, int q) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int kk = 4 * q + m;
+    const uint32_t a = a_tmem + 64u * q + 32u * (m >> 1) + 8u * (m & 1);
+    const uint64_t b = sdesc_add(db, static_cast<uint32_t>(kk) * 2048u);
+    if (m == 0 && !accumulate) mma_ts_c<0>(d_tmem, a, b, idesc);
+    else mma_ts_c<1>(d_tmem, a, b, idesc);
+  }
+}
+
 // Elementwise step of the dK/dV kernel on 32 query columns of one key row (column pairs packed
 // as f32x2): P^T = 2^(S^T c - lse2), dS^T = P^T (dP^T - D), both rounded to bf16 pairs.  MASK
 // (the diagonal tile only) zeroes P^T where the query precedes the key.
@@ -219,9 +237,12 @@ struct DkdvCfg : BwdCfg<D> {
   // stage: float4 per query-row pair {-lse2[2p], -lse2[2p+1], -D[2p], -D[2p+1]}, lse2 = lse * log2(e)
   static constexpr uint32_t OFF_VEC = OFF_RING + B::ST * STAGE;
   static constexpr uint32_t OFF_BAR = OFF_VEC + B::ST * B::VEC;
-  static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
-                       B_DRAIN = B_PF + 2, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;  // B_PF + c: chunk c of the
-                                                                               // elementwise step
+  // d = 64 takes each query tile in two halves of 64 queries (see the MMA issuer); d = 128 whole.
+  static constexpr bool HALVES = D == 64;
+  // B_SF (+ q): products (of query half q) ready; B_PF + c: elementwise chunk (half) c done;
+  // B_GF: gradients final
+  static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 2,
+                       B_GF = B_PF + 2, B_DRAIN = B_GF + 1, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
 };
@@ -260,8 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::B_EMPTY + s), 1);
     }
     mbar_init(BAR(C::B_SF), 1);
+    mbar_init(BAR(C::B_SF + 1), 1);
     mbar_init(BAR(C::B_PF), kEwWarps * 32);
     mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
+    mbar_init(BAR(C::B_GF), 1);
     mbar_init(BAR(C::B_DRAIN), 1);
     mbar_init(BAR(C::B_OW), kEwWarps * 32);  // bf16 gradients staged
     *abort_flag = 0;
@@ -323,43 +346,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_p = idesc_bf16_f32(kTile, kTile, 0);  // K Q^T, V dO^T: both K-major
-      constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);      // P^T dO, dS^T Q: MN-major B
-      const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
-      const uint64_t dR = sdesc_sw128(sRing, 16, 1024), dRmn = sdesc_sw128(sRing, kBox, 1024);
-      auto products = [&](int i) {
-        const uint32_t st = (i % C::ST) * C::STAGE;
-        issue_product<D>(tmem + kColA, dK, sdesc_add(dR, st), idesc_p);           // S^T = K Q^T
-        issue_product<D>(tmem + kColB, dV, sdesc_add(dR, st + C::TB), idesc_p);   // dP^T = V dO^T
-      };
-      bool ok = bwait(BAR(C::B_KV), 0, abort_flag, budget) && bwait(BAR(C::B_FULL), 0, abort_flag, budget);
-      if (ok) {
-        tc_fence_after();
-        products(0);
-        tc_commit(BAR(C::B_SF));
-      }
-      for (int i = 0; ok && i < n_i; ++i) {
-        const uint32_t st = (i % C::ST) * C::STAGE;
-        bool part_ok = true;
-        for (int part = 0; part < 2; ++part) {  // each half as soon as the elementwise warps finish it
-          if (!bwait(BAR(C::B_PF + part), i & 1, abort_flag, budget)) {
-            part_ok = false;
-            break;
+      if constexpr (C::HALVES) {
+        // Each query tile is taken in two halves of 64 queries, so that the products of one half run
+        // on the tensor core while the elementwise warps work on the other: S^T_q and dP^T_q are
+        // columns 64q .. 64q + 63 of the S^T and dP^T accumulators.
+        constexpr uint32_t idesc_p = idesc_bf16_f32(kTile, kTile / 2, 0);  // K Q_q^T, V dO_q^T: both K-major
+        constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);          // P^T dO, dS^T Q: MN-major B
+        const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+        const uint64_t dR = sdesc_sw128(sRing, 16, 1024), dRmn = sdesc_sw128(sRing, kBox, 1024);
+        auto products = [&](int i, int q) {  // rows 64q .. 64q + 63 of Q_i and dO_i are N
+          const uint32_t st = (i % C::ST) * C::STAGE + static_cast<uint32_t>(q) * (kTile / 2) * 128u;
+          issue_product<D>(tmem + kColA + 64u * q, dK, sdesc_add(dR, st), idesc_p);          // S^T_q = K Q_q^T
+          issue_product<D>(tmem + kColB + 64u * q, dV, sdesc_add(dR, st + C::TB), idesc_p);  // dP^T_q = V dO_q^T
+        };
+        bool ok = bwait(BAR(C::B_KV), 0, abort_flag, budget) && bwait(BAR(C::B_FULL), 0, abort_flag, budget);
+        if (ok) {
+          tc_fence_after();
+          products(0, 0);
+          tc_commit(BAR(C::B_SF));
+          products(0, 1);
+          tc_commit(BAR(C::B_SF + 1));
+        }
+        for (int i = 0; ok && i < n_i; ++i) {
+          const uint32_t st = (i % C::ST) * C::STAGE;
+          for (int q = 0; ok && q < 2; ++q) {
+            if (!bwait(BAR(C::B_PF + q), i & 1, abort_flag, budget)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_grad_half<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0 || q > 0,
+                               q);  // dV += P^T_q dO_q
+            issue_grad_half<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0 || q > 0,
+                               q);  // dK += dS^T_q Q_q
+            if (q == 1) tc_commit(BAR(C::B_EMPTY + i % C::ST));  // Q_i, dO_i fully read
+            if (i + 1 < n_i) {
+              // half q of the next tile into the columns the gradient MMAs above read: they were
+              // issued first, and MMAs complete in issue order
+              if (q == 0 && !bwait(BAR(C::B_FULL + (i + 1) % C::ST), ((i + 1) / C::ST) & 1, abort_flag, budget)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              products(i + 1, q);
+              tc_commit(BAR(C::B_SF + q));
+            }
           }
-          tc_fence_after();
-          issue_grad_part<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0 || part > 0,
-                             part);  // dV += P^T dO
-          issue_grad_part<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0 || part > 0,
-                             part);  // dK += dS^T Q
         }
-        if (!part_ok) break;
-        tc_commit(BAR(C::B_EMPTY + i % C::ST));
-        if (i + 1 < n_i) {
-          if (!bwait(BAR(C::B_FULL + (i + 1) % C::ST), ((i + 1) / C::ST) & 1, abort_flag, budget)) break;
+        tc_commit(BAR(C::B_GF));  // the gradients final (when every MMA above is complete)
+      } else {
+        // d = 128: TMEM holds S^T, dP^T, dV and dK (4 x 128 columns), so the products of the
+        // next query tile start only after this tile's elementwise step; the gradient MMAs of
+        // each 32-column chunk start as soon as the elementwise warps finish it.
+        constexpr uint32_t idesc_p = idesc_bf16_f32(kTile, kTile, 0);  // K Q^T, V dO^T: both K-major
+        constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);      // P^T dO, dS^T Q: MN-major B
+        const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+        const uint64_t dR = sdesc_sw128(sRing, 16, 1024), dRmn = sdesc_sw128(sRing, kBox, 1024);
+        auto products = [&](int i) {
+          const uint32_t st = (i % C::ST) * C::STAGE;
+          issue_product<D>(tmem + kColA, dK, sdesc_add(dR, st), idesc_p);           // S^T = K Q^T
+          issue_product<D>(tmem + kColB, dV, sdesc_add(dR, st + C::TB), idesc_p);   // dP^T = V dO^T
+        };
+        bool ok = bwait(BAR(C::B_KV), 0, abort_flag, budget) && bwait(BAR(C::B_FULL), 0, abort_flag, budget);
+        if (ok) {
           tc_fence_after();
-          products(i + 1);
+          products(0);
+          tc_commit(BAR(C::B_SF));
         }
-        tc_commit(BAR(C::B_SF));  // next products ready (or the gradients final)
+        for (int i = 0; ok && i < n_i; ++i) {
+          const uint32_t st = (i % C::ST) * C::STAGE;
+          bool part_ok = true;
+          for (int part = 0; part < 2; ++part) {  // each half as soon as the elementwise warps finish it
+            if (!bwait(BAR(C::B_PF + part), i & 1, abort_flag, budget)) {
+              part_ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_grad_part<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0 || part > 0,
+                               part);  // dV += P^T dO
+            issue_grad_part<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0 || part > 0,
+                               part);  // dK += dS^T Q
+          }
+          if (!part_ok) break;
+          tc_commit(BAR(C::B_EMPTY + i % C::ST));
+          if (i + 1 < n_i) {
+            if (!bwait(BAR(C::B_FULL + (i + 1) % C::ST), ((i + 1) / C::ST) & 1, abort_flag, budget)) break;
+            tc_fence_after();
+            products(i + 1);
+          }
+          if (i + 1 < n_i) tc_commit(BAR(C::B_SF));  // next products ready
+        }
+        tc_commit(BAR(C::B_GF));  // the gradients final (when every MMA above is complete)
       }
       tc_commit(BAR(C::B_DRAIN));
       bdrain(BAR(C::B_DRAIN), 0, budget);
@@ -373,33 +450,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tA = tmem + lane_addr + kColA, tB = tmem + lane_addr + kColB;
     const uint64_t c2 = f2_pack(sl2, sl2);
     bool ok = true;
-    for (int i = 0; ok && i < n_i; ++i) {
-      const int s = i % C::ST;
-      ok = bwait_all(BAR(C::B_SF), i & 1, abort_flag, budget) &&
-           bwait_all(BAR(C::B_FULL + s), (i / C::ST) & 1, abort_flag, budget);
-      if (!ok) break;
-      tc_fence_after();
-      const int qt = i0 + i;
-      const float4* nv = reinterpret_cast<const float4*>(vec + s * (2 * kTile));
-      // Causal: only the diagonal query tile (qt == kt) holds pairs with query < key.
-      const bool diag = CAUSAL && qt == kt;
-      // this thread's 64 query columns, two chunks of 32
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], pv[32];
-        tmem_ld2_x32<64>(tA + 32 * c, sv);
-        tmem_ld2_x32<64>(tB + 32 * c, pv);
-        uint32_t pp[16], dp[16];
-        if (diag) ew_pairs_dkdv<true>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
-        else ew_pairs_dkdv<false>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
-        tmem_st2_x16<64>(tA + 16 * c, pp);  // P^T packed: columns 64h + 16c ..
-        tmem_st2_x16<64>(tB + 16 * c, dp);  // dS^T packed
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
+    if constexpr (C::HALVES) {
+      for (int i = 0; ok && i < n_i; ++i) {
+        const int s = i % C::ST;
+        ok = bwait_all(BAR(C::B_FULL + s), (i / C::ST) & 1, abort_flag, budget);  // the tile's -lse, -D
+        const int qt = i0 + i;
+        const float4* nv = reinterpret_cast<const float4*>(vec + s * (2 * kTile));
+        // Causal: only the diagonal query tile (qt == kt) holds pairs with query < key.
+        const bool diag = CAUSAL && qt == kt;
+        // query half q: this thread's 32 queries 64q + 32h .. (columns of S^T_q, dP^T_q)
+        for (int q = 0; ok && q < 2; ++q) {
+          ok = bwait_all(BAR(C::B_SF + q), i & 1, abort_flag, budget);
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t sv[32], pv[32];
+          tmem_ld2_x32<32>(tA + 64 * q, sv);
+          tmem_ld2_x32<32>(tB + 64 * q, pv);
+          uint32_t pp[16], dp[16];
+          if (diag) ew_pairs_dkdv<true>(sv, pv, nv, c2, 64 * q + 32 * h, qt * kTile, key, pp, dp);
+          else ew_pairs_dkdv<false>(sv, pv, nv, c2, 64 * q + 32 * h, qt * kTile, key, pp, dp);
+          tmem_st2_x16<32>(tA + 64 * q, pp);  // P^T packed: columns 64q + 32h .. + 15
+          tmem_st2_x16<32>(tB + 64 * q, dp);  // dS^T packed
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(BAR(C::B_PF + q));  // half q ready: its gradient MMAs may start
+        }
+      }
+    } else {
+      for (int i = 0; ok && i < n_i; ++i) {
+        const int s = i % C::ST;
+        ok = bwait_all(BAR(C::B_SF), i & 1, abort_flag, budget) &&
+             bwait_all(BAR(C::B_FULL + s), (i / C::ST) & 1, abort_flag, budget);
+        if (!ok) break;
+        tc_fence_after();
+        const int qt = i0 + i;
+        const float4* nv = reinterpret_cast<const float4*>(vec + s * (2 * kTile));
+        // Causal: only the diagonal query tile (qt == kt) holds pairs with query < key.
+        const bool diag = CAUSAL && qt == kt;
+        // this thread's 64 query columns, two chunks of 32
+  #pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32], pv[32];
+          tmem_ld2_x32<64>(tA + 32 * c, sv);
+          tmem_ld2_x32<64>(tB + 32 * c, pv);
+          uint32_t pp[16], dp[16];
+          if (diag) ew_pairs_dkdv<true>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
+          else ew_pairs_dkdv<false>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
+          tmem_st2_x16<64>(tA + 16 * c, pp);  // P^T packed: columns 64h + 16c ..
+          tmem_st2_x16<64>(tB + 16 * c, dp);  // dS^T packed
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
+        }
       }
     }
-    if (ok) ok = bwait_all(BAR(C::B_SF), n_i & 1, abort_flag, budget);  // gradients final
+    if (ok) ok = bwait_all(BAR(C::B_GF), 0, abort_flag, budget);  // gradients final
     if (ok) {
       tc_fence_after();
       const size_t row_off = static_cast<size_t>(bh) * N + key;

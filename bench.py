@@ -70,8 +70,8 @@ NCU_TRAFFIC = {
     ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 228.017e6,
                                    "sha256": "8ce9ad5fd573ae9ad5bde635e7bd1a79c3b5a1621a130322717c60d010a367ce"},
     # backward: the dominant kernel (dK/dV) on the causal workload
-    ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1060.249e6,
-                                    "sha256": "989af07c8d9f2cef598efdd2625961591aac3471fb8465e545ad689f6f41316b"},
+    ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1057.557e6,
+                                    "sha256": "9665478df47b6e03320993535010ca3dc6a918b193d8ddc2b76543d201cfd249"},
     # decode: captured on the B4 slice (decode_small) and scaled by 16 to B64 (K/V streamed once)
     ("decode_split_kernel", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2151.001e6,
                                         "sha256": "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"},

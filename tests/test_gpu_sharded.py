@@ -103,3 +103,15 @@ def test_sharded_causal_workload_sampled_rows():
     from _util import gather_rows
     o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, True, rows=rows.numpy())
     assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref, "sharded causal workload")
+
+
+def test_sharded_noncausal_d64_many_items_per_cta():
+    # non-causal d = 64 shards run on the persistent kernel: B4 H16 N2048 is 512 blocks per shard
+    # on at most 152 CTAs, so every CTA writes partials for several blocks in turn
+    B, H, N, d = 4, 16, 2048, 64
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=11, device=DEV)
+    o, lse, *_ = run_sharded(q, k, v, [0, 1000, 2048], 0.125, False, streams=True)
+    rows = inputs.sample_rows_per_head(B, H, N, 24, seed=12)
+    from _util import gather_rows
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), 0.125, False, rows=rows.numpy())
+    assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref, "sharded d64 non-causal")

@@ -42,7 +42,8 @@
 // (causal launches order the blocks longest first).  fwd_persist_kernel (non-causal bf16,
 // d = 64) runs one CTA per SM that walks a list of blocks, keeping TMEM, barriers and the K/V
 // ring between them, so that a block's Q load and first S overlap the previous block's last
-// steps and epilogue; it also runs the key pieces of fa_fwd_ex's tail split.
+// steps and epilogue; it also runs the split last round of fa_fwd_ex (key pieces or single query
+// tiles).
 //
 // Causal: key tiles above a query tile's diagonal are never computed for it
 // (Q_0 stops one tile before Q_1); only the diagonal tile masks (col > row ->
@@ -720,7 +721,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 // (blockIdx.x, + gridDim.x, ...).  An item is a block of 256 query rows (two tiles) of one (b, h)
 // against the keys koff .. koff + Nk - 1, loaded from key row kload; the blocks run in
 // (b*h, block) order.  The blocks from n_full on (a partly filled last round) may be cut: into
-// ksplit key pieces that leave partial (U, m, l) rows for the combine kernel (aux.lin, the tail
+// ksplit key pieces that leave partial (U, m, l) rows for the combine kernel (aux.lin, the key
 // split), or into their two query tiles, each an item of its own (aux.qsplit).  Between items a
 // CTA keeps its TMEM, barriers and K/V ring: the next Q is loaded as soon as the last S MMAs of
 // the current item have read Q, and the next item's S(0) is issued right after the current
@@ -785,7 +786,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  grid_dep_launch();  // a dependent kernel (the tail combine) may launch once every CTA has started
+  grid_dep_launch();  // a dependent kernel (a key split's combine) may launch once every CTA has started
   const int w0 = static_cast<int>(blockIdx.x), w_step = static_cast<int>(gridDim.x), n_items = aux.n_items;
 
   if (threadIdx.x == 0) {
@@ -1120,7 +1121,7 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
     return launch_kernel(fwd_persist_kernel<D>, grid, C::THREADS, PersistSmem::SMEM, stream, a.tq, a.tk, a.tv, a.o,
                          a.lse, a.N, a.scale_log2, a.o_fp32, a.budget, aux, a.to);
   } else {
-    // one CTA per block of 256 query rows (the tail split is planned for the persistent kernel only)
+    // one CTA per block of 256 query rows (a split last round is planned for the persistent kernel only)
     if (aux.lin) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
     return launch_kernel(fwd_kernel<D, CAUSAL, FP8>, grid, C::THREADS, C::SMEM, stream, a.tq, a.tk, a.tv, a.o, a.lse,

@@ -29,8 +29,8 @@ struct FwdAux {
   float* m_part;
   float* l_part;
   int shard, S;
-  // Tail split (lin = 1): a 1-D grid of work items over 256-row query blocks in (b*h, block)
-  // order.  Items [0, n_full) are whole blocks writing O and lse; each later block is split
+  // Key split of the last round (lin = 1; work items over 256-row query blocks in (b*h, block)
+  // order): items [0, n_full) are whole blocks writing O and lse; each later block is split
   // into ksplit key pieces of kchunk keys (items n_full + ksplit*(block - n_full) + piece),
   // and piece s of flat row r (= b*h*N + n) writes partial slot (r - prow0) * ksplit + s.
   int lin;
@@ -41,7 +41,7 @@ struct FwdAux {
   // Query split (persistent kernel, lin = 0): the blocks from n_full on run as two single-tile
   // items each (items n_full + 2*(block - n_full) + tile).
   int qsplit;
-  // Persistent CTAs (non-causal bf16): the number of work items; set by launch_fwd.
+  // Persistent CTAs (non-causal bf16 d = 64): the number of work items; set by launch_fwd.
   int n_items;
 };
 

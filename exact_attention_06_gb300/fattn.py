@@ -122,7 +122,7 @@ def _stream(stream):
 
 
 def fa_fwd_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool = False) -> int:
-    """Scratch bytes of fa_fwd_ex's tail split on the current device (0: no split planned)."""
+    """Scratch bytes of the key split of fa_fwd_ex's last round on the current device (0: no key split)."""
     return int(lib().fa_fwd_workspace_bytes(B, H, N, d, int(bool(causal))))
 
 
@@ -131,7 +131,7 @@ def fa_fwd_ex(q, k, v, o, lse, scale: float, causal: bool = False, stream=None, 
     """Fused forward: q, k, v, o [B, H, N, d]; lse [B, H, N] fp32.
 
     ``o`` may be bf16 (default) or fp32 (``o_fp32``, inferred from o's dtype).  ``workspace``:
-    an optional uint8 CUDA tensor of at least fa_fwd_workspace_bytes() bytes for the tail split.
+    an optional uint8 CUDA tensor of at least fa_fwd_workspace_bytes() bytes for the key split.
     """
     B, H, N, d = q.shape
     if o_fp32 is None:

@@ -54,7 +54,7 @@ typedef enum {
 typedef struct {
   int o_fp32;                            /* 0: O is bf16 (round to nearest even); 1: O is fp32 */
   unsigned long long wait_budget_cycles; /* per-wait spin budget in SM clock cycles; 0 = default (about 2 s) */
-  void* workspace;                       /* optional device scratch, 256-byte aligned, for the tail split
+  void* workspace;                       /* optional device scratch, 256-byte aligned, for the key split
                                             (fa_fwd_workspace_bytes); NULL: one launch, no split */
   size_t workspace_bytes;                /* its size in bytes */
 } fa_fwd_opts;
@@ -165,7 +165,7 @@ fa_status_t fa_quantize_e4m3(const void* x, void* codes, float* scales,
  *   o           [B, H, N, d] bf16 (fp32 with opts->o_fp32), 16-byte aligned.
  *   lse         [B, H, N] fp32 (written), as for fa_fwd.
  *   d           must be 128 (FA_ERR_UNSUPPORTED otherwise).
- *   scale, causal, opts: as for fa_fwd_ex (opts may be NULL; no tail split:
+ *   scale, causal, opts: as for fa_fwd_ex (opts may be NULL; no split last round:
  *               opts->workspace is not used).
  * Scores are S = (q8 k8^T) * sq_i * sk_j * scale in fp32; P~ of key tile j
  * is stored as E4M3 of p * 256 * sv_j / max_j(sv_j) (p <= 1 after the row

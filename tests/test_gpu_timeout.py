@@ -22,8 +22,9 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-# (d, causal, O dtype, tail split): the persistent d = 64 kernel with fp32 O (stored by each
-# thread) and with bf16 O (the staged TMA store) plus the tail split's key pieces and combine;
+# (d, causal, O dtype, key split): the persistent d = 64 kernel with fp32 O (stored by each
+# thread, the last round as single query tiles) and with bf16 O (the staged TMA store) plus the
+# key split's pieces and combine;
 # the one-block-per-CTA kernel at d = 128 causal
 @pytest.mark.parametrize("d,causal,o_fp32,tail", [(64, False, True, False), (64, False, False, True),
                                                   (128, True, True, False)])

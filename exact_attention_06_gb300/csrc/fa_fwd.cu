@@ -43,7 +43,8 @@
 // d = 64) runs one CTA per SM that walks a list of blocks, keeping TMEM, barriers and the K/V
 // ring between them, so that a block's Q load and first S overlap the previous block's last
 // steps and epilogue; it also runs the split last round of fa_fwd_ex (key pieces or single query
-// tiles).
+// tiles).  Its two MMA warps split the products by kind instead of by tile: one issues every
+// S_t, the other every PV_t.
 //
 // Causal: key tiles above a query tile's diagonal are never computed for it
 // (Q_0 stops one tile before Q_1); only the diagonal tile masks (col > row ->
@@ -724,9 +725,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 // ksplit key pieces that leave partial (U, m, l) rows for the combine kernel (aux.lin, the key
 // split), or into their two query tiles, each an item of its own (aux.qsplit).  Between items a
 // CTA keeps its TMEM, barriers and K/V ring: the next Q is loaded as soon as the last S MMAs of
-// the current item have read Q, and the next item's S(0) is issued right after the current
-// item's last PV, under the softmax warps' epilogue.  The step itself is the separate-P~
-// schedule of fwd_kernel at d = 64.
+// the current item have read Q, and the next item's S(0) is issued as soon as the softmax has
+// read the current item's last S, under its last steps and epilogue.  The step itself is the
+// separate-P~ schedule of fwd_kernel at d = 64, with the S and PV products issued by two threads
+// of their own.
 struct FwdItem {
   int bh, pair, koff, kload, Nk, n0, n1;
   bool to_part;
@@ -882,19 +884,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         drain_wait(BAR(C::B_VF + g % C::VST), (g / C::VST) & 1, budget);
     }
   } else if (warp == kWarpMma || warp == kWarpMma + 1) {
-    // ------------------------------------------------------------ MMA issuer of one tile
+    // ------------------------------------------------------------ MMA issuers
+    // One thread issues every S product (both tiles), the other every PV product, so that
+    // S_t(j+1) is never queued behind the issue of PV_t(j) and is ready when the softmax of
+    // step j ends.  The two tiles share each issuer in step order (tile 0's step before tile 1's).
     if (lane == 0) {
-      const int t = warp - kWarpMma;
+      const bool s_issuer = warp == kWarpMma;
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
-      const uint64_t dq = sdesc_add(sdesc_sw128(sQ, 16, 1024), t * C::QB);
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
-      const uint32_t d_s = tmem + t * kBc;
-      const uint32_t d_o = tmem + kColO + t * D;
-      const uint32_t a_p = tmem + C::COL_P + 64u * t;
-      auto issue_s = [&](int g) {  // S_t = Q_t K^T with K from ring stage g
+      auto issue_s = [&](int t, int g) {  // S_t = Q_t K^T with K from ring stage g
+        const uint64_t dq = sdesc_add(dq0, t * C::QB);
         const uint64_t dk = sdesc_add(dk0, (g % C::KST) * C::KVB);
+        const uint32_t d_s = tmem + t * kBc;
 #pragma unroll
         for (int kk = 0; kk < C::ROW / 32; ++kk) {  // 32 bytes of K per MMA
           const uint32_t off = static_cast<uint32_t>(kk & 3) * 32u;
@@ -902,8 +906,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
         }
       };
-      auto issue_pv = [&](int g, bool first) {  // U_t (+)= P~_t V with V from ring stage g
+      auto issue_pv = [&](int t, int g, bool first) {  // U_t (+)= P~_t V with V from ring stage g
         const uint64_t dv = sdesc_add(dv0, (g % C::VST) * C::KVB);
+        const uint32_t d_o = tmem + kColO + t * D;
+        const uint32_t a_p = tmem + C::COL_P + 64u * t;
 #pragma unroll
         for (int kk = 0; kk < kBc / C::K_MMA; ++kk) {  // 16 keys per MMA: 8 TMEM columns of P~
           const uint64_t b = sdesc_add(dv, static_cast<uint32_t>(kk * C::K_MMA) * 128u);
@@ -914,61 +920,66 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       auto wait = [&](uint32_t bar, uint32_t parity) {
         return mbar_wait(bar, parity, abort_flag, budget, &g_fwd_status);
       };
-      int g = 0, kc = 0;  // this tile's steps and the CTA's key tiles over the items so far
+      int g0 = 0, g1 = 0, kc = 0;  // each tile's steps and the CTA's key tiles over the items so far
       bool ok = true, issued = false;
       for (int w = w0, it = 0; ok && w < n_items; w += w_step, ++it) {
         const FwdItem I = item_at(w, aux, N);
-        const int n = t ? I.n1 : I.n0, n_max = max(I.n0, I.n1);
-        // This item's Q (waited for first in every case, so that this warp's release of Q below
-        // falls into this item's phase).
-        ok = wait(BAR(C::B_Q), it & 1);
-        if (!ok) break;
-        if (n == 0) {  // no rows of this tile in the item: release Q and every K/V stage unread
-          mbar_arrive(BAR(C::B_QE));
-          for (int j = 0; ok && j < n_max; ++j) {
-            const int gg = kc + j;
-            ok = wait(BAR(C::B_KF + gg % C::KST), (gg / C::KST) & 1);
-            if (ok) mbar_arrive(BAR(C::B_KE + gg % C::KST));
-            ok = ok && wait(BAR(C::B_VF + gg % C::VST), (gg / C::VST) & 1);
-            if (ok) mbar_arrive(BAR(C::B_VE + gg % C::VST));
-          }
-          kc += n_max;
-          continue;
-        }
-        // The previous item's last S read by the softmax, and this item's first K.
-        ok = (g == 0 || wait(BAR(C::B_SC + t), (g - 1) & 1)) && wait(BAR(C::B_KF + kc % C::KST), (kc / C::KST) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(kc);
-        issued = true;
-        tc_commit(BAR(C::B_SF + t));
-        tc_commit(BAR(C::B_KE + kc % C::KST));
-        if (n == 1) tc_commit(BAR(C::B_QE));  // the item's last S
-        for (int j = 0; ok && j < n; ++j) {
-          if (j + 1 < n) {  // S_t(j+1) as soon as the softmax has read S_t(j)
-            const int gk = kc + j + 1;
-            ok = wait(BAR(C::B_SC + t), (g + j) & 1) && wait(BAR(C::B_KF + gk % C::KST), (gk / C::KST) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(gk);
-            tc_commit(BAR(C::B_SF + t));
-            tc_commit(BAR(C::B_KE + gk % C::KST));
-            if (j + 2 == n) tc_commit(BAR(C::B_QE));
-          }
-          const int gv = kc + j;
-          ok = wait(BAR(C::B_PF + t), (g + j) & 1) && wait(BAR(C::B_VF + gv % C::VST), (gv / C::VST) & 1);
+        const int n_max = max(I.n0, I.n1);
+        if (s_issuer) {
+          // This item's Q; a tile with no rows in the item releases its share of Q at once and
+          // each K stage of the item unread.
+          ok = wait(BAR(C::B_Q), it & 1);
           if (!ok) break;
-          tc_fence_after();
-          issue_pv(gv, j == 0);
-          tc_commit(BAR(C::B_OF + t));
-          tc_commit(BAR(C::B_VE + gv % C::VST));
+          if (I.n0 == 0) mbar_arrive(BAR(C::B_QE));
+          if (I.n1 == 0) mbar_arrive(BAR(C::B_QE));
+          for (int j = 0; ok && j < n_max; ++j) {
+            const int gk = kc + j;
+            ok = wait(BAR(C::B_KF + gk % C::KST), (gk / C::KST) & 1);
+            for (int t = 0; ok && t < 2; ++t) {
+              const int n = t ? I.n1 : I.n0, gt = (t ? g1 : g0) + j;
+              if (n == 0) {
+                mbar_arrive(BAR(C::B_KE + gk % C::KST));
+                continue;
+              }
+              // S_t(j) overwrites S_t(j-1) (over items: the previous item's last S): read first
+              ok = gt == 0 || wait(BAR(C::B_SC + t), (gt - 1) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(t, gk);
+              issued = true;
+              tc_commit(BAR(C::B_SF + t));
+              tc_commit(BAR(C::B_KE + gk % C::KST));
+              if (j + 1 == n) tc_commit(BAR(C::B_QE));  // the tile's last S of the item
+            }
+          }
+        } else {
+          for (int j = 0; ok && j < n_max; ++j) {
+            const int gv = kc + j;
+            ok = wait(BAR(C::B_VF + gv % C::VST), (gv / C::VST) & 1);
+            for (int t = 0; ok && t < 2; ++t) {
+              const int n = t ? I.n1 : I.n0, gt = (t ? g1 : g0) + j;
+              if (n == 0) {
+                mbar_arrive(BAR(C::B_VE + gv % C::VST));
+                continue;
+              }
+              ok = wait(BAR(C::B_PF + t), gt & 1);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, gv, j == 0);
+              issued = true;
+              tc_commit(BAR(C::B_OF + t));
+              tc_commit(BAR(C::B_VE + gv % C::VST));
+            }
+          }
         }
-        g += n;
+        g0 += I.n0;
+        g1 += I.n1;
         kc += n_max;
       }
       if (issued) {  // all MMAs complete before TMEM is released
-        tc_commit(BAR(C::B_DRAIN + t));
-        drain_wait(BAR(C::B_DRAIN + t), 0, budget);
+        const int b = s_issuer ? 0 : 1;
+        tc_commit(BAR(C::B_DRAIN + b));
+        drain_wait(BAR(C::B_DRAIN + b), 0, budget);
       }
     }
   } else {

@@ -794,8 +794,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
     mbar_init(BAR(C::B_QE), 2);
-    // Each K (V) stage is released once by each tile's MMA warp; a tile with no rows in an item
-    // releases the item's stages without reading them.
+    // Each K (V) stage is released once per tile, by the S (PV) issuer; for a tile with no rows in
+    // an item the issuer releases the item's stages without reading them.
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(BAR(C::B_KF + s), 1);
       mbar_init(BAR(C::B_KE + s), 2);

@@ -43,8 +43,9 @@
 // d = 64) runs one CTA per SM that walks a list of blocks, keeping TMEM, barriers and the K/V
 // ring between them, so that a block's Q load and first S overlap the previous block's last
 // steps and epilogue; it also runs the split last round of fa_fwd_ex (key pieces or single query
-// tiles).  Its two MMA warps split the products by kind instead of by tile: one issues every
-// S_t, the other every PV_t.
+// tiles).  It has three MMA-issuing threads: the S products of both tiles, the PV products of
+// tile 0, those of tile 1 (an issuing thread keeps about one batch of MMAs in flight, so PV_0 and
+// PV_1 from threads of their own overlap).
 //
 // Causal: key tiles above a query tile's diagonal are never computed for it
 // (Q_0 stops one tile before Q_1); only the diagonal tile masks (col > row ->
@@ -112,14 +113,25 @@ struct FwdCfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;  // TMEM address slot, abort flag
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;   // + slack to align the base to 1 KB
 };
-// The persistent kernel (bf16 d = 64) adds O of both tiles, staged for the TMA store (128 bytes a row).
-struct PersistSmem {
-  static constexpr uint32_t OFF_O = (FwdCfg<64>::OFF_MISC + 16u + 1023u) & ~1023u;
+// The persistent kernel (bf16 d = 64): the d = 64 layout with three MMA-issuing warps (the S
+// products of both tiles, the PV products of tile 0, those of tile 1) before the producer, a
+// drain barrier for each, and O of both tiles staged in shared memory for the TMA store (128
+// bytes a row).  20 warps are five per SMSP: 96 registers a thread.
+struct PersistCfg : FwdCfg<64> {
+  static constexpr int N_ISSUERS = 3;
+  static constexpr int WARP_TMA = kWarpMma + N_ISSUERS;
+  static constexpr int THREADS = (WARP_TMA + 1) * 32;
+  static constexpr int B_Q = 0, B_QE = B_Q + 1, B_KF = B_QE + 1, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
+                       B_SF = B_VE + VST, B_PF = B_SF + 2, B_SC = B_PF + 2, B_OF = B_SC + 2, B_DRAIN = B_OF + 2,
+                       B_OSF = B_DRAIN + N_ISSUERS, B_OW = B_OSF + 2, NBAR = B_OW + 2;
+  static constexpr uint32_t OFF_BAR = OFF_V + VST * KVB;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
+  static constexpr uint32_t OFF_O = (OFF_MISC + 16u + 1023u) & ~1023u;
   static constexpr uint32_t SMEM = OFF_O + 2u * kBr * 128u + 1024u;
 };
 static_assert(FwdCfg<128>::SMEM <= 232448, "shared memory of the d=128 kernel exceeds 227 KB");
 static_assert(FwdCfg<128, true>::SMEM <= 232448, "shared memory of the FP8 kernel exceeds 227 KB");
-static_assert(PersistSmem::SMEM <= 232448, "shared memory of the persistent kernel exceeds 227 KB");
+static_assert(PersistCfg::SMEM <= 232448, "shared memory of the persistent kernel exceeds 227 KB");
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long budget) {
@@ -727,8 +739,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 // CTA keeps its TMEM, barriers and K/V ring: the next Q is loaded as soon as the last S MMAs of
 // the current item have read Q, and the next item's S(0) is issued as soon as the softmax has
 // read the current item's last S, under its last steps and epilogue.  The step itself is the
-// separate-P~ schedule of fwd_kernel at d = 64, with the S and PV products issued by two threads
-// of their own.
+// separate-P~ schedule of fwd_kernel at d = 64, with the S products issued by one thread and
+// each tile's PV products by a thread of its own.
 struct FwdItem {
   int bh, pair, koff, kload, Nk, n0, n1;
   bool to_part;
@@ -770,13 +782,13 @@ __device__ __forceinline__ FwdItem item_at(int w, const FwdAux& aux, int N) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+__global__ void __launch_bounds__(PersistCfg::THREADS, 1)
     fwd_persist_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, void* __restrict__ o, float* __restrict__ lse,
                        int N, float sl2, int o_fp32, unsigned long long budget, const FwdAux aux,
                        const __grid_constant__ CUtensorMap to) {
-  using C = FwdCfg<D>;
-  static_assert(D == 64 && C::SEP && C::TWO_ISSUERS && !C::P_SMEM, "the persistent forward is the d = 64 schedule");
+  using C = PersistCfg;
+  static_assert(D == 64 && C::SEP && !C::P_SMEM, "the persistent forward is the d = 64 schedule");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -794,8 +806,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
     mbar_init(BAR(C::B_QE), 2);
-    // Each K (V) stage is released once per tile, by the S (PV) issuer; for a tile with no rows in
-    // an item the issuer releases the item's stages without reading them.
+    // Each K (V) stage is released once per tile, by the S issuer (the tile's PV issuer); for a
+    // tile with no rows in an item the issuer releases the item's stages without reading them.
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(BAR(C::B_KF + s), 1);
       mbar_init(BAR(C::B_KE + s), 2);
@@ -810,8 +822,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(BAR(C::B_SC + t), kSoftmaxWarps * 32);
       mbar_init(BAR(C::B_OF + t), 1);
     }
-    mbar_init(BAR(C::B_DRAIN), 1);
-    mbar_init(BAR(C::B_DRAIN + 1), 1);
+    for (int i = 0; i < C::N_ISSUERS; ++i) mbar_init(BAR(C::B_DRAIN + i), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR(C::B_OSF + t), 1);                 // O staging of tile t free again
       mbar_init(BAR(C::B_OW + t), kSoftmaxWarps * 32);  // O staging of tile t written
@@ -883,13 +894,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int g = max(0, v_issued - C::VST); g < v_issued; ++g)
         drain_wait(BAR(C::B_VF + g % C::VST), (g / C::VST) & 1, budget);
     }
-  } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+  } else if (warp >= kWarpMma && warp < kWarpMma + C::N_ISSUERS) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread issues every S product (both tiles), the other every PV product, so that
-    // S_t(j+1) is never queued behind the issue of PV_t(j) and is ready when the softmax of
-    // step j ends.  The two tiles share each issuer in step order (tile 0's step before tile 1's).
+    // Three threads: the S products of both tiles (tile 0's step before tile 1's), the PV
+    // products of tile 0, those of tile 1, so that no PV issue waits behind the other tile's.
+    // S_t(j+1) goes out as soon as the softmax has read S_t(j); PV_t(j) as soon as P~_t(j) is
+    // stored.
     if (lane == 0) {
-      const bool s_issuer = warp == kWarpMma;
+      const int role = warp - kWarpMma;
+      const bool s_issuer = role == 0;
+      const int t_pv = role - 1;  // the PV issuer's tile
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
@@ -953,23 +967,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
           }
         } else {
+          const int t = t_pv, n = t ? I.n1 : I.n0, g = t ? g1 : g0;
           for (int j = 0; ok && j < n_max; ++j) {
             const int gv = kc + j;
             ok = wait(BAR(C::B_VF + gv % C::VST), (gv / C::VST) & 1);
-            for (int t = 0; ok && t < 2; ++t) {
-              const int n = t ? I.n1 : I.n0, gt = (t ? g1 : g0) + j;
-              if (n == 0) {
-                mbar_arrive(BAR(C::B_VE + gv % C::VST));
-                continue;
-              }
-              ok = wait(BAR(C::B_PF + t), gt & 1);
-              if (!ok) break;
-              tc_fence_after();
-              issue_pv(t, gv, j == 0);
-              issued = true;
-              tc_commit(BAR(C::B_OF + t));
-              tc_commit(BAR(C::B_VE + gv % C::VST));
+            if (!ok) break;
+            if (n == 0) {
+              mbar_arrive(BAR(C::B_VE + gv % C::VST));
+              continue;
             }
+            ok = wait(BAR(C::B_PF + t), (g + j) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, gv, j == 0);
+            issued = true;
+            tc_commit(BAR(C::B_OF + t));
+            tc_commit(BAR(C::B_VE + gv % C::VST));
           }
         }
         g0 += I.n0;
@@ -977,9 +990,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         kc += n_max;
       }
       if (issued) {  // all MMAs complete before TMEM is released
-        const int b = s_issuer ? 0 : 1;
-        tc_commit(BAR(C::B_DRAIN + b));
-        drain_wait(BAR(C::B_DRAIN + b), 0, budget);
+        tc_commit(BAR(C::B_DRAIN + role));
+        drain_wait(BAR(C::B_DRAIN + role), 0, budget);
       }
     }
   } else {
@@ -997,7 +1009,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // bf16 O leaves through shared memory and one TMA store per tile and item, issued by the
     // tile's first thread; fp32 O and partials are stored by each thread.
     const bool o_issuer = (warp % kSoftmaxWarps) == 0 && lane == 0;
-    const uint32_t o_stage = base + PersistSmem::OFF_O + static_cast<uint32_t>(t) * (kBr * 128u);
+    const uint32_t o_stage = base + C::OFF_O + static_cast<uint32_t>(t) * (kBr * 128u);
     int g = 0;   // this tile's steps over the items so far: the phases of its SF and OF barriers
     int gi = 0;  // this tile's O tiles staged so far: the phases of its OSF and OW barriers
     bool ok = true;
@@ -1129,7 +1141,7 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
     if (items > INT_MAX) return cudaErrorInvalidValue;
     aux.n_items = static_cast<int>(items);
     const dim3 grid(static_cast<unsigned>(a.sms > 0 ? std::min<long long>(items, a.sms) : items));
-    return launch_kernel(fwd_persist_kernel<D>, grid, C::THREADS, PersistSmem::SMEM, stream, a.tq, a.tk, a.tv, a.o,
+    return launch_kernel(fwd_persist_kernel<D>, grid, PersistCfg::THREADS, PersistCfg::SMEM, stream, a.tq, a.tk, a.tv, a.o,
                          a.lse, a.N, a.scale_log2, a.o_fp32, a.budget, aux, a.to);
   } else {
     // one CTA per block of 256 query rows (a split last round is planned for the persistent kernel only)

@@ -63,12 +63,12 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 50.512e6,
-                                        "sha256": "59c348749fc0802cca8241d7c1d2afcf255e7a76cef52a1e83935cd7545b5504"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 591.096e6,
-                               "sha256": "59c348749fc0802cca8241d7c1d2afcf255e7a76cef52a1e83935cd7545b5504"},
-    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 228.365e6,
-                                   "sha256": "59c348749fc0802cca8241d7c1d2afcf255e7a76cef52a1e83935cd7545b5504"},
+    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 50.479e6,
+                                        "sha256": "32a08b4e555135e1a6c90b1b162b73995a64443a37d046425cc1ea391c7f9829"},
+    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 592.020e6,
+                               "sha256": "32a08b4e555135e1a6c90b1b162b73995a64443a37d046425cc1ea391c7f9829"},
+    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 226.991e6,
+                                   "sha256": "32a08b4e555135e1a6c90b1b162b73995a64443a37d046425cc1ea391c7f9829"},
     # backward: the dominant kernel (dK/dV) on the causal workload
     ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1057.557e6,
                                     "sha256": "9665478df47b6e03320993535010ca3dc6a918b193d8ddc2b76543d201cfd249"},

@@ -2,21 +2,22 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One JSON line on rank 0.  The headline workload is the prefill configuration
-(B=4, H=16, N=2048, d=64, non-causal, bf16): one step is one fa_fwd_ex call over
-it (the persistent fused forward; its 512 blocks of 256 query rows fill 3.37
-rounds of the 152 SMs, so the last round's 56 blocks run as 112 single query
-tiles), timed with CUDA events on the launching stream, L2 flushed (256 MiB
-write) between timed steps because its inputs (50 MB) fit in L2.
-``extra`` carries the other workloads of the target (causal N=8192 d=128 with
-x8 key spikes, ragged causal N=16381, split-KV decode L=32768) and of the
-library's further paths (backward and FP8 forward on the causal workload, the
-decode over a paged cache, the causal workload in four key shards merged by the
-combine), each with its roofline fraction; their inputs exceed L2.  ``e2e`` repeats the headline
-through the C ABI with pinned host buffers and the host<->device copies
-inside the timed region.  ``cpu_baseline`` is the fp64 oracle timed on the
-host cores over a bounded sample.  ``--impl reference`` times that oracle
-as the reference arm (there is no runnable reference implementation).
+One JSON line on rank 0.  The headline workload is the largest single-GPU
+configuration, the long ragged causal prefill (B=1, H=32, N=16381, d=128,
+causal, bf16): one step is one fa_fwd_ex call over it (one launch of the fused
+forward, 2048 blocks of 256 query rows, longest first), timed with CUDA events
+on the launching stream; its inputs (402 MB) exceed L2, so nothing is flushed.
+``extra`` carries the other workloads of the target (prefill N=2048 d=64 with
+L2 flushed between steps, causal N=8192 d=128 with x8 key spikes, split-KV
+decode L=32768) and of the library's further paths (backward and FP8 forward on
+the causal workload, the decode over a paged cache, the causal workload in four
+key shards merged by the combine), each with its roofline fraction.  ``e2e``
+repeats the headline through the C ABI with pinned host buffers and the
+host<->device copies inside the timed region.  ``cpu_baseline`` is the fp64
+oracle timed on the host cores (one thread and all of them) over a bounded
+sample of the headline's rows, with a labelled extrapolation to the whole
+workload.  ``--impl reference`` times that oracle as the reference arm (there
+is no runnable reference implementation).
 
 Multi-GPU: the work does not shard across GPUs in this design; under torchrun
 every rank runs an independent replica ("scaling": "weak") and the slowest
@@ -40,8 +41,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "prefill"
-EXTRA = ("causal", "ragged", "decode")
+HEADLINE = "ragged"
+EXTRA = ("prefill", "causal", "decode")
+E2E_CHUNKS = 8  # host<->device pipeline stages of the e2e step
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "attention fwd TFLOPS (bf16, causal/non-causal) and decode GB/s vs GB300 roofline"
 
@@ -78,6 +80,22 @@ NCU_TRAFFIC = {
     ("decode_split_kernel_paged", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2150.928e6,
                                               "sha256": "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"},
 }
+
+
+def _workload_label(w):
+    if w.kind == "decode":
+        return f"decode B{w.B} H{w.H} L{w.N} d{w.d}"
+    return (f"{w.name} B{w.B} H{w.H} N{w.N} d{w.d} {'causal' if w.causal else 'non-causal'}"
+            f"{' x8 key spikes' if w.spike else ''}")
+
+
+def _headline_config(w, world):
+    """The headline's config object, the same for both arms."""
+    l2 = "flushed between timed steps (256 MiB write)" if _fits_l2(w) else (
+        f"inputs larger than L2 ({3 * w.B * w.H * w.N * w.d * 2 / 1e6:.0f} MB of q, k, v): not flushed")
+    return {"workload": _workload_label(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": w.scale, "global_batch": w.B * world, "seq_len": w.N, "parallelism": f"replicas x{world}",
+            "l2": l2}
 
 
 def _traffic(kernel: str, workload: str):
@@ -180,6 +198,16 @@ def _dist():
 
 
 # ----------------------------------------------------------------------------- our arm
+
+def _fits_l2(w):
+    """Whether a prefill workload's q, k, v fit in L2 (then L2 is flushed between timed steps)."""
+    return w.kind == "prefill" and 3 * w.B * w.H * w.N * w.d * 2 < L2_FLUSH_BYTES
+
+
+def _fwd_kernel_name(w):
+    """The forward kernel fa_fwd_ex launches for a workload (bf16)."""
+    return "fwd_persist_kernel" if (not w.causal and w.d == 64) else "fwd_kernel"
+
 
 def _prefill_step_fn(w, dev, stream):
     import torch
@@ -362,42 +390,45 @@ def _roofline(kind, work_per_launch, launch_ms, peaks, traffic):
 def _e2e_prefill(w, dev, stream, steps, warmup):
     """Headline metric through the C ABI from pinned host buffers (copies timed).
 
-    The batch is processed in per-sequence chunks on three streams: the host-to-device copies of
-    q, k, v for chunk b+1 run while chunk b's fa_fwd_ex computes and chunk b-1's o, lse travel
-    back, so that the step costs about the input copies plus one chunk's compute and output copy
-    (the copies alone take ~3x the forward)."""
+    The B*H heads are processed in E2E_CHUNKS chunks of consecutive heads on three streams: the
+    host-to-device copies of q, k, v for chunk c+1 run while chunk c's fa_fwd_ex computes and
+    chunk c-1's o, lse travel back, so that the step costs about the copies plus one chunk's
+    compute (the copies alone take longer than the forward)."""
     import torch
     from exact_attention_06_gb300 import fattn, inputs
-    qh, kh, vh = (t.pin_memory() for t in inputs.workload_inputs(w, seed=0, device="cpu"))
-    oh = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
-    lh = torch.empty(w.B, w.H, w.N, dtype=torch.float32).pin_memory()
+    bh = w.B * w.H
+    n_chunks = E2E_CHUNKS if bh % E2E_CHUNKS == 0 else w.B
+    hc = bh // n_chunks  # heads per chunk
+    qh, kh, vh = (t.pin_memory().view(bh, w.N, w.d) for t in inputs.workload_inputs(w, seed=0, device="cpu"))
+    oh = torch.empty((bh, w.N, w.d), dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((bh, w.N), dtype=torch.float32).pin_memory()
     qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
     od = torch.empty_like(qd)
-    ld = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
-    chunk = inputs.Workload(w.name, w.kind, 1, w.H, w.N, w.d, w.causal)
-    ws = _tail_workspace(chunk, dev)
+    ld = torch.empty((bh, w.N), dtype=torch.float32, device=dev)
+    ws = _tail_workspace(inputs.Workload(w.name, w.kind, 1, hc, w.N, w.d, w.causal), dev)
     s_in, s_fwd, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
 
     def step():
         start = torch.cuda.Event()
         start.record(stream)
         s_in.wait_event(start)
-        for b in range(w.B):
+        for c in range(n_chunks):
+            sl = slice(c * hc, (c + 1) * hc)
             with torch.cuda.stream(s_in):
-                qd[b].copy_(qh[b], non_blocking=True)
-                kd[b].copy_(kh[b], non_blocking=True)
-                vd[b].copy_(vh[b], non_blocking=True)
+                qd[sl].copy_(qh[sl], non_blocking=True)
+                kd[sl].copy_(kh[sl], non_blocking=True)
+                vd[sl].copy_(vh[sl], non_blocking=True)
                 e_in = torch.cuda.Event()
                 e_in.record(s_in)
             s_fwd.wait_event(e_in)
-            fattn.fa_fwd_ex(qd[b:b + 1], kd[b:b + 1], vd[b:b + 1], od[b:b + 1], ld[b:b + 1], w.scale, w.causal,
-                            stream=s_fwd, workspace=ws)
+            fattn.fa_fwd_ex(qd[sl].unsqueeze(0), kd[sl].unsqueeze(0), vd[sl].unsqueeze(0), od[sl].unsqueeze(0),
+                            ld[sl].unsqueeze(0), w.scale, w.causal, stream=s_fwd, workspace=ws)
             e_fwd = torch.cuda.Event()
             e_fwd.record(s_fwd)
             s_out.wait_event(e_fwd)
             with torch.cuda.stream(s_out):
-                oh[b].copy_(od[b], non_blocking=True)
-                lh[b].copy_(ld[b], non_blocking=True)
+                oh[sl].copy_(od[sl], non_blocking=True)
+                lh[sl].copy_(ld[sl], non_blocking=True)
         done = torch.cuda.Event()
         done.record(s_out)
         stream.wait_event(done)
@@ -408,7 +439,7 @@ def _e2e_prefill(w, dev, stream, steps, warmup):
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
     return {"value": round(w.flops() / (t * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(t, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": f"{w.B} per-sequence chunks; H2D, fa_fwd_ex and D2H on three streams"}
+            "pipeline": f"{n_chunks} chunks of {hc} heads; H2D, fa_fwd_ex and D2H on three streams"}
 
 
 def run_ours(args):
@@ -443,7 +474,8 @@ def run_ours(args):
     step, launches = _prefill_step_fn(w, dev, stream)
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
-    ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush, sampler=sampler, dist_sync=dist_sync)
+    ms = _time_steps(step, args.steps, args.warmup, stream, flush=flush if _fits_l2(w) else None, sampler=sampler,
+                     dist_sync=dist_sync)
     sampler.stop()
     t_local = statistics.mean(ms)
     t = max_over_ranks(t_local, dist, dev)
@@ -458,14 +490,16 @@ def run_ours(args):
                 st_fn, nl = _decode_step_fn(we, dev, stream)
             else:
                 st_fn, nl = _prefill_step_fn(we, dev, stream)
-            ems = _time_steps(st_fn, args.extra_steps, max(3, args.warmup), stream, dist_sync=dist_sync)
+            small = _fits_l2(we)
+            ems = _time_steps(st_fn, args.extra_steps, max(3, args.warmup), stream, flush=flush if small else None,
+                              dist_sync=dist_sync)
             et = statistics.mean(ems)
             if we.kind == "decode":
                 work, kind, kern = we.kv_bytes(), "hbm", "decode_split_kernel"
                 val = work / (et * 1e-3) / 1e9
                 unit = "GB/s"
             else:
-                work, kind, kern = we.flops(), "tensor", "fwd_kernel"
+                work, kind, kern = we.flops(), "tensor", _fwd_kernel_name(we)
                 val = work / (et * 1e-3) / 1e12
                 unit = "TFLOP/s"
             extra[name] = {"value": round(val * world, 3), "unit": unit, "ms_per_step": round(et, 4),
@@ -473,7 +507,7 @@ def run_ours(args):
                            "config": {"B": we.B, "H": we.H, "N" if we.kind == "prefill" else "L": we.N, "d": we.d,
                                       "causal": we.causal, "spike_every_64th_key_x8": we.spike},
                            "roofline": _roofline(kind, work, et, peaks, _traffic(kern, name)),
-                           "l2": "inputs larger than L2"}
+                           "l2": "flushed between timed steps (256 MiB write)" if small else "inputs larger than L2"}
             if we.kind == "decode":
                 extra[name]["roofline"]["note"] = "duration covers the split kernel and the combine kernel"
             del st_fn
@@ -558,13 +592,11 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded iid N(0,1) bf16)",
-        "config": {"workload": "prefill B4 H16 N2048 d64 non-causal", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "scale": w.scale, "global_batch": w.B * world, "seq_len": w.N,
-                   "parallelism": f"replicas x{world}", "l2": "flushed between timed steps (256 MiB write)"},
+        "config": _headline_config(w, world),
         "gpu_launches": launches * args.steps,
-        "roofline": dict(_roofline("tensor", flops, t_local, peaks, _traffic("fwd_persist_kernel", HEADLINE)),
-                         note="duration covers the step's launches (the forward kernel, and the combine when "
-                              "the last round is split by keys); traffic is the forward kernel's"),
+        "roofline": dict(_roofline("tensor", flops, t_local, peaks, _traffic(_fwd_kernel_name(w), HEADLINE)),
+                         note=f"one {_fwd_kernel_name(w)} launch per step; flops 4*B*H*N^2*d"
+                              f"{' / 2 (causal)' if w.causal else ''}, traffic its DRAM bytes per launch"),
         "clocks": sampler.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -613,55 +645,83 @@ import oracle
 from exact_attention_06_gb300 import inputs
 w = inputs.WORKLOADS[{name!r}]
 steps, per_step, rows_per_call = {steps!r}, {per_step!r}, {rows!r}
-q, k, v = inputs.workload_inputs(w, seed=0, device="cpu")
+heads = min(w.H, 2)  # rows are sampled from the first heads: every head has the same shape
+q, k, v = inputs.prefill_inputs(1, heads, w.N, w.d, seed=0, device="cpu", spike=w.spike)
 out = []
 calls = 0
 for _ in range(steps):
-    done_rows = 0
+    done_rows, flops = 0, 0.0
     t0 = time.perf_counter()
     while True:
-        b, h = calls % w.B, (calls // w.B) % w.H
-        rows = inputs.sample_rows(w.N, rows_per_call, seed=calls)
-        oracle.attention_head(q[b, h], k[b, h], v[b, h], w.scale, w.causal, rows=rows.numpy())
+        h = calls % heads
+        rows = inputs.sample_rows(w.N, rows_per_call, seed=calls).numpy()
+        oracle.attention_head(q[0, h], k[0, h], v[0, h], w.scale, w.causal, rows=rows)
         done_rows += len(rows)
+        # algorithmic flops of the evaluated rows: 4*d per admissible key
+        flops += 4.0 * w.d * float(np.sum(rows + 1 if w.causal else np.full(len(rows), w.N)))
         calls += 1
         el = time.perf_counter() - t0
         if el >= per_step:
             break
-    # algorithmic flops of the evaluated rows: 4*d per admissible key (non-causal: all N keys)
-    out.append({{"seconds": el, "rows": done_rows, "flops": done_rows * 4.0 * w.N * w.d}})
+    out.append({{"seconds": el, "rows": done_rows, "flops": flops}})
 print(json.dumps(out))
 """
 
 
-def _oracle_steps(w, steps, per_step_s, rows):
-    """Run the fp64 oracle as it stands in a fresh process: `steps` bounded samples of the workload."""
+def _oracle_steps(w, steps, per_step_s, rows, threads=None):
+    """Run the fp64 oracle as it stands in a fresh process with `threads` BLAS threads (default: every
+    core of this process's affinity): `steps` bounded samples of the workload's rows."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    threads = threads or cores
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[var] = str(cores)
+        env[var] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
     script = _CPU_SAMPLE_SCRIPT.format(root=ROOT, name=w.name, steps=int(steps), per_step=float(per_step_s),
                                        rows=int(rows))
     r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, env=env,
-                       timeout=120 + steps * (per_step_s + 30))
+                       timeout=180 + steps * (per_step_s + 30))
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-500:])
-    return json.loads(r.stdout.strip().splitlines()[-1]), cores
+    return json.loads(r.stdout.strip().splitlines()[-1]), threads
+
+
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return None
 
 
 def cpu_baseline(w, budget_s=12.0, rows=256):
-    """The fp64 oracle on the host cores over a bounded sample (~budget_s seconds) of the workload."""
+    """The fp64 oracle on the host cores over bounded samples (~budget_s seconds each) of the
+    workload's rows: once on every core of the affinity mask (the reported value) and once on one
+    thread, each with seconds per row and a labelled extrapolation to the whole workload."""
+    legs = {}
     try:
-        res, cores = _oracle_steps(w, 1, budget_s, rows)
+        for label, threads in (("all_cores", None), ("one_thread", 1)):
+            res, used = _oracle_steps(w, 1, budget_s, rows, threads)
+            r = res[0]
+            rate = r["flops"] / r["seconds"]
+            legs[label] = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": used,
+                           "seconds": round(r["seconds"], 2), "rows": r["rows"],
+                           "seconds_per_row": round(r["seconds"] / r["rows"], 6),
+                           "extrapolated_full_workload_s": round(w.flops() / rate, 1)}
     except (RuntimeError, subprocess.TimeoutExpired) as e:
         return {"value": None, "unit": "TFLOP/s", "kind": "oracle", "error": str(e)[-300:]}
-    r = res[0]
-    return {"value": round(r["flops"] / r["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"{r['rows']} seeded query rows of the {w.name} workload ({rows} rows per call, explicit fp64 "
-                      f"score rows) in {r['seconds']:.1f} s; numpy/BLAS threads={cores}",
-            "seconds": round(r["seconds"], 2)}
+    a = legs["all_cores"]
+    return {"value": a["value"], "unit": "TFLOP/s", "cores": a["cores"], "kind": "oracle",
+            "sample": f"{a['rows']} seeded query rows of the {_workload_label(w)} workload ({rows} rows per call, "
+                      f"explicit fp64 score rows, drawn from its first heads) in {a['seconds']:.1f} s on "
+                      f"{a['cores']} numpy/BLAS threads; the same for one thread below",
+            "seconds": a["seconds"], "seconds_per_row": a["seconds_per_row"],
+            "extrapolated_full_workload_s": a["extrapolated_full_workload_s"],
+            "extrapolation": "labelled extrapolation: the whole workload's algorithmic flops at the sampled rate",
+            "one_thread": legs["one_thread"], "cpu_model": _cpu_model()}
 
 
 def run_reference(args):
@@ -682,11 +742,12 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000.0 * secs / len(timed), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded iid N(0,1) bf16)",
-        "config": {"workload": "prefill B4 H16 N2048 d64 non-causal", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "parallelism": "single process on host cores"},
+        "config": _headline_config(w, world),
+        "arm": "the fp64 oracle as it stands, single process on the host cores",
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: seeded query rows of the prefill workload for {per_step:.2f} s "
-                                   f"(64 rows per call, explicit fp64 score rows); numpy/BLAS threads={cores}"},
+                         "sample": f"each step: seeded query rows of the {_workload_label(w)} workload for "
+                                   f"{per_step:.2f} s (64 rows per call, explicit fp64 score rows); "
+                                   f"numpy/BLAS threads={cores}"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -465,11 +465,13 @@ size_t fa_decode_workspace_bytes(int B, int H, int L, int d, int chunk, int spli
   return plan.total();
 }
 
-fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
-                              int d, float scale, int chunk, int splits, void* workspace, size_t ws_bytes,
-                              void* stream) {
+fa_status_t fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                 int L, int d, float scale, int chunk, int splits, void* workspace, size_t ws_bytes,
+                                 void* stream, const fa_decode_opts* opts) {
   g_last_error[0] = '\0';
   if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  const int o_fp32 = opts ? opts->o_fp32 : 0;
+  if (o_fp32 != 0 && o_fp32 != 1) return fail(FA_ERR_INVALID_ARG, "opts->o_fp32 must be 0 or 1");
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
@@ -509,14 +511,21 @@ fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void*
   a.splits = plan.splits;
   a.keys_per_split = plan.keys_per_split;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.budget = kDefaultBudget;
+  a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
   cudaGetLastError();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fattn::launch_decode_split(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv split launch");
-  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, 0, s);
+  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, o_fp32, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv combine launch");
   return FA_OK;
+}
+
+fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int L,
+                              int d, float scale, int chunk, int splits, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  return fa_decode_splitkv_ex(q, k, v, o, lse, B, H, L, d, scale, chunk, splits, workspace, ws_bytes, stream,
+                              nullptr);
 }
 
 fa_status_t fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -533,6 +542,21 @@ fa_status_t fa_decode_splitkv_noalloc(const void* q, const void* k, const void* 
     if ((st = plan_decode(B, H, L, d, chunk, 1, 0, &plan)) != FA_OK) return st;
     if ((st = check_device(&sms)) != FA_OK) return st;
     if ((st = plan_decode(B, H, L, d, chunk, 0, sms, &plan)) != FA_OK) return st;
+  }
+  if (splits == 0 && plan.total() > fattn::kNoAllocScratchBytes) {
+    // The automatic plan does not fit: take the largest smaller split count (that leaves no split
+    // empty) whose partials fit.
+    const int n_chunks = (L + chunk - 1) / chunk;
+    for (int s = plan.splits - 1; s >= 1; --s) {
+      const int cps = (n_chunks + s - 1) / s;
+      if ((n_chunks + cps - 1) / cps != s) continue;
+      DecodePlan p2;
+      if ((st = plan_decode(B, H, L, d, chunk, s, 0, &p2)) != FA_OK) return st;
+      if (p2.total() <= fattn::kNoAllocScratchBytes) {
+        plan = p2;
+        break;
+      }
+    }
   }
   if (plan.total() > fattn::kNoAllocScratchBytes)
     return fail(FA_ERR_WORKSPACE,
@@ -560,13 +584,15 @@ size_t fa_decode_paged_workspace_bytes(int B, int H, int max_seq_len, int d, int
   return st == FA_OK ? plan.total() : 0;
 }
 
-fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
-                            const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size,
-                            int max_pages, int num_pages, int max_seq_len, float scale, int splits, void* workspace,
-                            size_t ws_bytes, void* stream) {
+fa_status_t fa_decode_paged_ex(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                               const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size,
+                               int max_pages, int num_pages, int max_seq_len, float scale, int splits,
+                               void* workspace, size_t ws_bytes, void* stream, const fa_decode_opts* opts) {
   g_last_error[0] = '\0';
   if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o || !lse)
     return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  const int o_fp32 = opts ? opts->o_fp32 : 0;
+  if (o_fp32 != 0 && o_fp32 != 1) return fail(FA_ERR_INVALID_ARG, "opts->o_fp32 must be 0 or 1");
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16))
     return fail(FA_ERR_INVALID_ARG, "q, k_pages, v_pages and o must be 16-byte aligned");
@@ -609,7 +635,7 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
   a.splits = plan.splits;
   a.keys_per_split = plan.keys_per_split;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.budget = kDefaultBudget;
+  a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.H = H;
@@ -620,15 +646,24 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fattn::launch_decode_split(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged split launch");
-  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, 0, s);
+  e = fattn::launch_combine(a.u_part, a.m_part, a.l_part, o, lse, a.BH, a.splits, d, o_fp32, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged combine launch");
   return FA_OK;
 }
 
-fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
-                       int S, int d, void* stream) {
+fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                            const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size,
+                            int max_pages, int num_pages, int max_seq_len, float scale, int splits, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  return fa_decode_paged_ex(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, H, d, page_size, max_pages,
+                            num_pages, max_seq_len, scale, splits, workspace, ws_bytes, stream, nullptr);
+}
+
+fa_status_t fa_combine_ex(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
+                          int S, int d, int o_fp32, void* stream) {
   g_last_error[0] = '\0';
   if (!u_part || !m_part || !l_part || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (o_fp32 != 0 && o_fp32 != 1) return fail(FA_ERR_INVALID_ARG, "o_fp32 must be 0 or 1");
   if (R < 1 || S < 1) return fail(FA_ERR_INVALID_ARG, "R and S must be >= 1 (got %d, %d)", R, S);
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
   if (!aligned(u_part, 16) || !aligned(o, 16)) return fail(FA_ERR_INVALID_ARG, "u_part and o must be 16-byte aligned");
@@ -637,9 +672,15 @@ fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_
   fa_status_t st = check_device(nullptr);
   if (st != FA_OK) return st;
   cudaGetLastError();
-  cudaError_t e = fattn::launch_combine(u_part, m_part, l_part, o, lse, R, S, d, 0, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      fattn::launch_combine(u_part, m_part, l_part, o, lse, R, S, d, o_fp32, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_combine launch");
   return FA_OK;
+}
+
+fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part, void* o, float* lse, int R,
+                       int S, int d, void* stream) {
+  return fa_combine_ex(u_part, m_part, l_part, o, lse, R, S, d, 0, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N) {

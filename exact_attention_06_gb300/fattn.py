@@ -25,10 +25,11 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes",
-            "fa_decode_splitkv", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes", "fa_decode_paged",
-            "fa_combine", "fa_get_status", "fa_status_string",
-            "fa_last_error")
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8",
+            "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes", "fa_decode_splitkv",
+            "fa_decode_splitkv_ex", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes",
+            "fa_decode_paged", "fa_decode_paged_ex", "fa_combine", "fa_combine_ex", "fa_get_status",
+            "fa_status_string", "fa_last_error")
 FA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -41,6 +42,10 @@ class FattnError(RuntimeError):
 class FaFwdOpts(ctypes.Structure):
     _fields_ = [("o_fp32", ctypes.c_int), ("wait_budget_cycles", ctypes.c_ulonglong),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class FaDecodeOpts(ctypes.Structure):
+    _fields_ = [("o_fp32", ctypes.c_int), ("wait_budget_cycles", ctypes.c_ulonglong)]
 
 
 _lib = None
@@ -67,19 +72,24 @@ def lib() -> ctypes.CDLL:
         L.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.fa_decode_workspace_bytes.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+        L.fa_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp,
+                                           ctypes.POINTER(FaDecodeOpts)]
         L.fa_decode_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         L.fa_decode_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         L.fa_decode_paged_workspace_bytes.restype = sz
         L.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+        L.fa_decode_paged_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp,
+                                         ctypes.POINTER(FaDecodeOpts)]
         L.fa_combine.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+        L.fa_combine_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
         L.fa_get_status.argtypes = [vp]
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd", "fa_decode_splitkv",
-                     "fa_decode_splitkv_noalloc", "fa_decode_paged",
-                     "fa_combine", "fa_get_status"):
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd",
+                     "fa_decode_splitkv", "fa_decode_splitkv_ex", "fa_decode_splitkv_noalloc", "fa_decode_paged",
+                     "fa_decode_paged_ex", "fa_combine", "fa_combine_ex", "fa_get_status"):
             getattr(L, name).restype = i
         _lib = L
     return _lib
@@ -202,21 +212,25 @@ def fa_decode_workspace_bytes(B: int, H: int, L: int, d: int, chunk: int = 128, 
     return int(lib().fa_decode_workspace_bytes(B, H, L, d, chunk, splits))
 
 
-def fa_decode_splitkv(q, k, v, o, lse, scale: float, workspace, chunk: int = 128, splits: int = 0, stream=None):
-    """Split-KV decode: q [B, H, d], k/v [B, H, L, d], o [B, H, d], lse [B, H]; workspace a uint8 CUDA tensor."""
+def fa_decode_splitkv(q, k, v, o, lse, scale: float, workspace, chunk: int = 128, splits: int = 0, stream=None,
+                      wait_budget_cycles: int = 0):
+    """Split-KV decode: q [B, H, d], k/v [B, H, L, d], o [B, H, d] bf16 or fp32 (from its dtype),
+    lse [B, H]; workspace a uint8 CUDA tensor (fa_decode_splitkv_ex)."""
     B, H, L, d = k.shape
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale), chunk,
-                                 splits, _ptr(workspace), ws_bytes, _stream(stream))
-    _check(st, "fa_decode_splitkv")
+    opts = FaDecodeOpts(int(o.dtype == torch.float32), int(wait_budget_cycles))
+    st = lib().fa_decode_splitkv_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale), chunk,
+                                    splits, _ptr(workspace), ws_bytes, _stream(stream), ctypes.byref(opts))
+    _check(st, "fa_decode_splitkv_ex")
 
 
 def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, chunk: int = 128, splits: int = 0, stream=None):
     """fa_decode_splitkv without a workspace, for callers that cannot allocate device memory.
 
-    The partials go to a fixed 8 MiB device array inside the library; larger
-    requests raise FattnError(FA_ERR_WORKSPACE).  Calls that overlap on the GPU
-    share that array and race: keep them on one stream.
+    The partials go to a fixed 8 MiB device array inside the library; with
+    splits=0 the split count is lowered until they fit, an explicit count that
+    does not fit raises FattnError(FA_ERR_WORKSPACE).  Calls that overlap on the
+    GPU share that array and race: keep them on one stream.
     """
     B, H, L, d = k.shape
     st = lib().fa_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale),
@@ -230,9 +244,10 @@ def fa_decode_paged_workspace_bytes(B: int, H: int, max_seq_len: int, d: int, pa
 
 
 def fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale: float, max_seq_len: int,
-                    workspace=None, splits: int = 0, stream=None):
+                    workspace=None, splits: int = 0, stream=None, wait_budget_cycles: int = 0):
     """Split-KV decode over a paged cache: q [B, H, d]; k_pages/v_pages [P, H, page_size, d];
-    block_table [B, max_pages] int32; seq_lens [B] int32; o [B, H, d] bf16; lse [B, H] fp32."""
+    block_table [B, max_pages] int32; seq_lens [B] int32; o [B, H, d] bf16 or fp32 (from its
+    dtype); lse [B, H] fp32 (fa_decode_paged_ex)."""
     B, H, d = q.shape
     P, _, page_size, _ = k_pages.shape
     max_pages = block_table.shape[1]
@@ -240,17 +255,20 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale: f
         workspace = torch.empty(fa_decode_paged_workspace_bytes(B, H, max_seq_len, d, page_size, max_pages, splits),
                                 dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o),
-                               _ptr(lse), B, H, d, page_size, max_pages, P, max_seq_len, float(scale), splits,
-                               _ptr(workspace), ws_bytes, _stream(stream))
-    _check(st, "fa_decode_paged")
+    opts = FaDecodeOpts(int(o.dtype == torch.float32), int(wait_budget_cycles))
+    st = lib().fa_decode_paged_ex(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o),
+                                  _ptr(lse), B, H, d, page_size, max_pages, P, max_seq_len, float(scale), splits,
+                                  _ptr(workspace), ws_bytes, _stream(stream), ctypes.byref(opts))
+    _check(st, "fa_decode_paged_ex")
 
 
 def fa_combine(u_part, m_part, l_part, o, lse, stream=None):
-    """Merge partials: u_part [R, S, d], m_part/l_part [R, S] fp32 -> o [R, d] bf16, lse [R] fp32."""
+    """Merge partials: u_part [R, S, d], m_part/l_part [R, S] fp32 -> o [R, d] bf16 or fp32 (from its
+    dtype; fa_combine_ex), lse [R] fp32."""
     R, S, d = u_part.shape
-    st = lib().fa_combine(_ptr(u_part), _ptr(m_part), _ptr(l_part), _ptr(o), _ptr(lse), R, S, d, _stream(stream))
-    _check(st, "fa_combine")
+    st = lib().fa_combine_ex(_ptr(u_part), _ptr(m_part), _ptr(l_part), _ptr(o), _ptr(lse), R, S, d,
+                             int(o.dtype == torch.float32), _stream(stream))
+    _check(st, "fa_combine_ex")
 
 
 def fa_get_status(stream=None) -> int:

@@ -177,6 +177,16 @@ fa_status_t fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
                        void* o, float* lse, int B, int H, int N, int d, float scale,
                        int causal, void* stream, const fa_fwd_opts* opts);
 
+/* Options of fa_decode_splitkv_ex and fa_decode_paged_ex.  A zero-initialised
+ * struct (or NULL) gives the behaviour of the entry points without _ex. */
+typedef struct {
+  int o_fp32;                            /* 0: O is bf16 (round to nearest even); 1: O is fp32 [B, H, d] */
+  unsigned long long wait_budget_cycles; /* per-wait spin budget of the split kernel in SM clock
+                                            cycles; 0 = default (about 2 s).  A wait that runs out
+                                            ends the kernel and fa_get_status() reports
+                                            FA_ERR_TIMEOUT; O and lse are then undefined. */
+} fa_decode_opts;
+
 /*
  * fa_decode_workspace_bytes -- bytes of scratch that fa_decode_splitkv needs.
  *
@@ -213,6 +223,13 @@ fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void*
                               int B, int H, int L, int d, float scale, int chunk, int splits,
                               void* workspace, size_t ws_bytes, void* stream);
 
+/* fa_decode_splitkv with options (opts may be NULL): opts->o_fp32 = 1 makes `o`
+ * an fp32 [B, H, d] tensor (16-byte aligned); opts->wait_budget_cycles bounds
+ * each wait of the split kernel. */
+fa_status_t fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int L, int d, float scale, int chunk, int splits,
+                                 void* workspace, size_t ws_bytes, void* stream, const fa_decode_opts* opts);
+
 /*
  * fa_decode_splitkv_noalloc -- fa_decode_splitkv for callers that cannot
  * allocate device memory.  (The pages have no counterpart to this entry
@@ -229,10 +246,15 @@ fa_status_t fa_decode_splitkv(const void* q, const void* k, const void* v, void*
  *
  *   Arguments as fa_decode_splitkv, without workspace and ws_bytes.
  *   The partials of B*H rows with S splits take
- *   fa_decode_workspace_bytes(B, H, L, d, chunk, S) bytes; a request larger
- *   than FA_NOALLOC_SCRATCH_BYTES returns FA_ERR_WORKSPACE (fa_last_error()
- *   says by how much) and launches nothing.  B*H*S*(d+2)*4 bytes is about the
- *   need: e.g. B*H = 2048 rows at d = 128 fit up to 7 splits.
+ *   fa_decode_workspace_bytes(B, H, L, d, chunk, S) bytes; B*H*S*(d+2)*4 bytes
+ *   is about the need: e.g. B*H = 2048 rows at d = 128 fit up to 7 splits.
+ *   With splits = 0 the split count is the automatic one of fa_decode_splitkv
+ *   when its partials fit, else the largest smaller count whose partials fit
+ *   (O and lse are the same function of q, k, v either way, up to rounding
+ *   order).  An explicit split count whose partials do not fit, or B*H rows
+ *   that do not fit even with one split (more than 16131 rows at d = 128),
+ *   return FA_ERR_WORKSPACE (fa_last_error() says by how much) and launch
+ *   nothing.
  *   Every GPU that loads the library's decode code holds the 8 MiB array until
  *   the process exits.  The first call on each device looks up the array's
  *   device address (cudaGetSymbolAddress) with that device current; make that
@@ -284,6 +306,12 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
                             int B, int H, int d, int page_size, int max_pages, int num_pages,
                             int max_seq_len, float scale, int splits, void* workspace,
                             size_t ws_bytes, void* stream);
+/* fa_decode_paged with options (opts may be NULL), as for fa_decode_splitkv_ex. */
+fa_status_t fa_decode_paged_ex(const void* q, const void* k_pages, const void* v_pages,
+                               const int* block_table, const int* seq_lens, void* o, float* lse,
+                               int B, int H, int d, int page_size, int max_pages, int num_pages,
+                               int max_seq_len, float scale, int splits, void* workspace,
+                               size_t ws_bytes, void* stream, const fa_decode_opts* opts);
 
 /*
  * fa_combine -- merge S partial (U, m, l) triples per row into O and lse:
@@ -302,6 +330,10 @@ fa_status_t fa_decode_paged(const void* q, const void* k_pages, const void* v_pa
  */
 fa_status_t fa_combine(const float* u_part, const float* m_part, const float* l_part,
                        void* o, float* lse, int R, int S, int d, void* stream);
+/* fa_combine with the output type chosen: o_fp32 = 0 writes o [R, d] bf16
+ * (round to nearest even), o_fp32 = 1 writes o [R, d] fp32 (16-byte aligned). */
+fa_status_t fa_combine_ex(const float* u_part, const float* m_part, const float* l_part,
+                          void* o, float* lse, int R, int S, int d, int o_fp32, void* stream);
 
 /*
  * fa_bwd_workspace_bytes -- scratch bytes fa_bwd needs: the per-row

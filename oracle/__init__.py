@@ -11,6 +11,7 @@ from .attention import (  # noqa: F401
     attention_fp8,
     attention_fp8_head,
     attention_backward_head,
+    attention_backward_rows,
     attention_head,
     backward_delta,
     chunk_partials,

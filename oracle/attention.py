@@ -37,6 +37,10 @@ What it computes, and where the pages define it
   (triton-tutorial "8. FlashAttention 实战", §8.8.1 gradient formulas and
   §8.8.3 D_i and dS; operatorworld "反向传播：用重算换显存").  P is formed
   explicitly here; the blockwise recomputation from lse is the GPU's business.
+* ``attention_backward_rows`` -- the same gradients at selected query rows (dQ)
+  and key rows (dK, dV) of one head, forming only those rows and columns of
+  P, dP and dS (plus every row's softmax normaliser and D_i), for heads too
+  long for the full N x N matrices.
 * ``e4m3_values`` / ``quantize_e4m3_blocks`` / ``dequantize_blocks`` -- FP8
   block quantization (triton-tutorial "8. FlashAttention 实战", §8.9.4: one
   scale per 128-row block, scale = max|x| / 448, E4M3 max 448): the scale and
@@ -415,6 +419,67 @@ def attention_backward(q, k, v, do, scale: float, causal: bool = False):
         for h in range(q.shape[1]):
             dq[b, h], dk[b, h], dv[b, h] = attention_backward_head(q[b, h], k[b, h], v[b, h], do[b, h], scale,
                                                                    causal)
+    return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, do, scale: float, causal: bool = False, q_rows=None, k_rows=None,
+                            block: int = 512):
+    """Gradients of one head at selected rows, fp64: dQ for the query rows ``q_rows``, dK and dV for
+    the key rows ``k_rows`` (either may be None).
+
+    The definitions of ``attention_backward_head`` (triton-tutorial §8.8.1: dV = P^T dO,
+    dP = dO V^T; §8.8.3: D_i = sum_j P_ij dP_ij, dS = P (dP - D); dQ = scale dS K,
+    dK = scale dS^T Q), restricted to those rows and columns so that a head of 8192 rows fits in
+    memory.  dS_ij needs every query row's softmax normaliser and D_i, so the score rows of all
+    queries are formed first (``block`` rows at a time) for m_i = max_j s_ij,
+    l_i = sum_j exp(s_ij - m_i) and D_i; then the selected rows (dQ) or columns (dK, dV) of
+    P = exp(s - m) / l, dP and dS are formed explicitly and contracted.  A query row with no
+    admissible key has P = 0 and zero gradients.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    n, nk = q.shape[0], k.shape[0]
+    scale = float(scale)
+    m = np.full(n, NEG_INF)
+    l = np.zeros(n)
+    dd = np.zeros(n)
+
+    def scores(rows, cols):
+        s = scale * (q[rows] @ k[cols].T)
+        if causal:
+            s = np.where(cols[None, :] > rows[:, None], NEG_INF, s)
+        return s
+
+    def probs(rows, cols):
+        s = scores(rows, cols)
+        base = np.where(np.isfinite(m[rows]), m[rows], 0.0)
+        e = np.exp(s - base[:, None])  # masked scores give exp(-inf) = 0
+        return e / np.where(l[rows] > 0, l[rows], 1.0)[:, None]
+
+    all_keys = np.arange(nk)
+    for r0 in range(0, n, block):
+        rows = np.arange(r0, min(n, r0 + block))
+        s = scores(rows, all_keys)
+        mx = s.max(axis=1) if nk > 0 else np.full(rows.shape[0], NEG_INF)
+        base = np.where(np.isfinite(mx), mx, 0.0)
+        e = np.exp(s - base[:, None])
+        m[rows] = mx
+        l[rows] = e.sum(axis=1)
+        p = e / np.where(l[rows] > 0, l[rows], 1.0)[:, None]
+        dd[rows] = (p * (do[rows] @ v.T)).sum(axis=1)
+
+    dq = dk = dv = None
+    if q_rows is not None:
+        rows = np.asarray(q_rows, dtype=np.int64)
+        p = probs(rows, all_keys)
+        ds = p * ((do[rows] @ v.T) - dd[rows][:, None])
+        dq = scale * (ds @ k)
+    if k_rows is not None:
+        cols = np.asarray(k_rows, dtype=np.int64)
+        all_rows = np.arange(n)
+        p = probs(all_rows, cols)  # column j of P for every query row
+        ds = p * ((do @ v[cols].T) - dd[:, None])
+        dv = p.T @ do
+        dk = scale * (ds.T @ q)
     return dq, dk, dv
 
 

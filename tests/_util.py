@@ -50,11 +50,17 @@ def bf16_half_ulp(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def assert_parity(o, lse, o_ref, lse_ref, what=""):
-    """fp32 O: the bounds apply to |O - O_ref| directly.  bf16 O: they apply to
-    what remains after the output's own round-to-nearest (half a bf16 ulp),
-    i.e. O must be the bf16 rounding of a value that meets the fp32 bounds."""
-    is_bf16 = getattr(o, "dtype", None) == torch.bfloat16
+def assert_parity(o, lse, o_ref, lse_ref, what="", raw=False):
+    """The bounds max|O - O_ref| <= 1e-2, mean <= 1e-3, max|lse - lse_ref| <= 1e-3.
+
+    fp32 O: applied to |O - O_ref| as it is.  bf16 O with ``raw``: applied as
+    it is too (used where |O| is small enough that bf16's own rounding stays
+    well inside the bounds, e.g. decode over long caches, |O| ~ 0.03).  bf16 O
+    without ``raw``: applied to what remains after the output's own
+    round-to-nearest (half a bf16 ulp), i.e. O must be the bf16 rounding of a
+    value that meets the bounds; every such check has an fp32-O twin that is
+    held to the raw bounds."""
+    is_bf16 = getattr(o, "dtype", None) == torch.bfloat16 and not raw
     o_np = o.detach().cpu().double().numpy()
     lse_np = lse.detach().cpu().double().numpy()
     assert np.all(np.isfinite(o_np)), f"{what}: non-finite O"

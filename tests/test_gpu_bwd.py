@@ -88,3 +88,25 @@ def test_backward_deterministic_and_identities_at_full_causal_size():
     sum_do = do.double().sum(dim=2)
     assert float((sum_dv - sum_do).abs().max()) <= 2e-2 * float(sum_do.abs().max())
     assert float(dk.sum(dim=2).abs().max()) <= 2e-2 * float(dk.abs().sum(dim=2).max())
+
+
+def test_backward_full_causal_size_sampled_rows_against_the_oracle():
+    """B2 H16 N8192 d128 causal with x8 key spikes (the bench's backward workload), as the bench runs
+    it (bf16 gradients) and with fp32 gradients: on two seeded heads, dQ at 64 seeded query rows and
+    dK, dV at 64 seeded key rows (plus tile-edge rows) against the fp64 oracle restricted to those
+    rows, which forms every query row's softmax statistics and the keys' full score columns."""
+    w = inputs.WORKLOADS["causal"]
+    q, k, v = inputs.workload_inputs(w, seed=0, device=DEV)
+    do = inputs.normal_bf16(q.shape, seed=9, device=DEV)
+    grads = {dt: run_bwd(q, k, v, do, w.scale, True, grad_fp32=dt) for dt in (True, False)}
+    heads = [(int(i) // w.H, int(i) % w.H) for i in inputs.sample_rows(w.B * w.H, 2, seed=21)]
+    edge = [0, 1, 127, 128, 4095, 4096, w.N - 129, w.N - 128, w.N - 1]
+    for n, (b, h) in enumerate(heads):
+        qr = np.unique(np.concatenate([inputs.sample_rows(w.N, 64, seed=30 + n).numpy(), edge]))
+        kr = np.unique(np.concatenate([inputs.sample_rows(w.N, 64, seed=40 + n).numpy(), edge]))
+        dq_ref, dk_ref, dv_ref = oracle.attention_backward_rows(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(),
+                                                                do[b, h].cpu(), w.scale, True, q_rows=qr, k_rows=kr)
+        qi, ki = torch.from_numpy(qr).to(DEV), torch.from_numpy(kr).to(DEV)
+        for fp32, (dq, dk, dv) in grads.items():
+            got = (dq[b, h].index_select(0, qi), dk[b, h].index_select(0, ki), dv[b, h].index_select(0, ki))
+            assert_grads(got, (dq_ref, dk_ref, dv_ref), f"full causal b={b} h={h} grad_fp32={fp32}")

@@ -1,11 +1,11 @@
 """Failure detection on the GPU, without a fault: every wait in the kernels is
 bounded, and a wait that runs out ends the kernel with a status the host reads.
 
-fa_fwd_ex with a one-cycle wait budget makes the first waits of every CTA run
-out (the data they wait for cannot arrive within one cycle).  The kernel must
-report FA_ERR_TIMEOUT through fa_get_status, drain its in-flight copies and
-MMAs, free its TMEM, and leave the context usable: the next normal call on the
-same inputs must be correct.
+fa_fwd_ex (and fa_decode_splitkv_ex / fa_decode_paged_ex) with a one-cycle wait
+budget makes the first waits of every CTA run out (the data they wait for
+cannot arrive within one cycle).  The kernel must report FA_ERR_TIMEOUT through
+fa_get_status, drain its in-flight copies (and MMAs), free its TMEM, and leave
+the context usable: the next normal call on the same inputs must be correct.
 """
 
 import math
@@ -51,3 +51,38 @@ def test_wait_budget_expiry_is_reported_and_the_context_survives(d, causal, o_fp
                                       rows=inputs.sample_rows(N, 256, seed=1).numpy())
     rows = inputs.sample_rows(N, 256, seed=1)
     assert_parity(o2[:, :, rows], lse2[:, :, rows], o_ref, lse_ref, "after a timeout")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_wait_budget_expiry_is_reported_and_the_context_survives(paged):
+    ensure_built()
+    B, H, L, d, ps = 2, 4, 4992, 128, 128  # 39 pages of 128 keys per sequence
+    q, k, v = inputs.decode_inputs(B, H, L, d, seed=31, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    n = L // ps
+    if paged:
+        kp = k.view(B, H, n, ps, d).permute(0, 2, 1, 3, 4).reshape(B * n, H, ps, d).contiguous()
+        vp = v.view(B, H, n, ps, d).permute(0, 2, 1, 3, 4).reshape(B * n, H, ps, d).contiguous()
+        table = torch.arange(B * n, dtype=torch.int32, device=DEV).view(B, n)
+        lens = torch.full((B,), L, dtype=torch.int32, device=DEV)
+
+    def call(o, lse, budget):
+        if paged:
+            fattn.fa_decode_paged(q, kp, vp, table, lens, o, lse, scale, L, wait_budget_cycles=budget)
+        else:
+            ws = torch.empty(fattn.fa_decode_workspace_bytes(B, H, L, d, 128, 0), dtype=torch.uint8, device=DEV)
+            fattn.fa_decode_splitkv(q, k, v, o, lse, scale, ws, 128, 0, wait_budget_cycles=budget)
+
+    o = torch.zeros(B, H, d, dtype=torch.float32, device=DEV)
+    lse = torch.zeros(B, H, dtype=torch.float32, device=DEV)
+    call(o, lse, 1)
+    with pytest.raises(fattn.FattnError) as err:
+        fattn.fa_get_status()
+    assert err.value.status == fattn.FA_ERR_TIMEOUT
+    assert fattn.fa_get_status() == fattn.FA_OK  # the status word was cleared by the read
+    o2 = torch.full((B, H, d), float("nan"), dtype=torch.float32, device=DEV)
+    lse2 = torch.full((B, H), float("nan"), dtype=torch.float32, device=DEV)
+    call(o2, lse2, 0)
+    assert fattn.fa_get_status() == fattn.FA_OK
+    o_ref, lse_ref = oracle.decode(q.cpu(), k.cpu(), v.cpu(), scale)
+    assert_parity(o2.reshape(B * H, d), lse2.reshape(B * H), o_ref, lse_ref, f"decode after a timeout paged={paged}")

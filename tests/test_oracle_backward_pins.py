@@ -97,3 +97,36 @@ def test_batched_wrapper():
     np.testing.assert_allclose(dq[1, 2], dq1)
     np.testing.assert_allclose(dk[1, 2], dk1)
     np.testing.assert_allclose(dv[1, 2], dv1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_restricted_gradients_match_torch_autograd(causal):
+    """attention_backward_rows at seeded query and key rows equals torch fp64 autograd's full
+    gradients at those rows; with a block smaller than N the row statistics span several blocks."""
+    n, d = 53, 8
+    q, k, v, do = (RNG.standard_normal((n, d)) for _ in range(4))
+    scale = 1 / math.sqrt(d)
+    tq, tk, tv = _loss_grads_torch(q, k, v, do, scale, causal)
+    qr = np.array([0, 1, 17, 30, 52])
+    kr = np.array([0, 5, 26, 51, 52])
+    for block in (7, 512):
+        dq, dk, dv = oracle.attention_backward_rows(q, k, v, do, scale, causal, q_rows=qr, k_rows=kr, block=block)
+        np.testing.assert_allclose(dq, tq[qr], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(dk, tk[kr], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(dv, tv[kr], rtol=1e-11, atol=1e-12)
+
+
+def test_row_restricted_last_key_closed_form():
+    """Causal, last key j = N-1: only row N-1 attends it, so dV_j = P_{N-1,j} dO_{N-1} and
+    dK_j = scale * dS_{N-1,j} q_{N-1} (a closed form from one explicit softmax row)."""
+    n, d = 12, 4
+    q, k, v, do = (RNG.standard_normal((n, d)) for _ in range(4))
+    scale = 0.6
+    s = scale * q[-1] @ k.T
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    dp = v @ do[-1]
+    ds = p * (dp - (p * dp).sum())
+    _, dk, dv = oracle.attention_backward_rows(q, k, v, do, scale, True, k_rows=[n - 1])
+    np.testing.assert_allclose(dv[0], p[-1] * do[-1], rtol=1e-12)
+    np.testing.assert_allclose(dk[0], scale * ds[-1] * q[-1], rtol=1e-12, atol=1e-14)

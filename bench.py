@@ -63,23 +63,36 @@ def _peaks():
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
-# under profiles/, keyed by kernel and workload, valid only while the kernel source is unchanged.
+# under profiles/, keyed by kernel and workload, valid only while the kernel sources are unchanged.
+_FWD = "28ed220eca2dba6a16cd3f446b682c83b7699c938c09a55c43c2a9464f4ae862"
+_BWD = "6d749b47961456b4b380118c44a2749a4a5aeeb8a964204b8b9e57beca829f47"
+_DEC = "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"
 NCU_TRAFFIC = {
-    ("fwd_persist_kernel", "prefill"): {"source": "fa_fwd.cu", "bytes": 50.479e6,
-                                        "sha256": "32a08b4e555135e1a6c90b1b162b73995a64443a37d046425cc1ea391c7f9829"},
-    ("fwd_kernel", "causal"): {"source": "fa_fwd.cu", "bytes": 592.020e6,
-                               "sha256": "32a08b4e555135e1a6c90b1b162b73995a64443a37d046425cc1ea391c7f9829"},
-    ("fwd_kernel_fp8", "causal"): {"source": "fa_fwd.cu", "bytes": 226.991e6,
-                                   "sha256": "32a08b4e555135e1a6c90b1b162b73995a64443a37d046425cc1ea391c7f9829"},
+    ("fwd_kernel", "ragged"): {"sources": {"fa_fwd.cu": _FWD}, "bytes": 553.953e6},
+    ("fwd_kernel", "causal"): {"sources": {"fa_fwd.cu": _FWD}, "bytes": 260.98e6},
+    ("fwd_kernel_fp8", "causal"): {"sources": {"fa_fwd.cu": _FWD}, "bytes": 138.22e6},
     # backward: the dominant kernel (dK/dV) on the causal workload
-    ("bwd_dkdv_kernel", "causal"): {"source": "fa_bwd.cu", "bytes": 1057.557e6,
-                                    "sha256": "9665478df47b6e03320993535010ca3dc6a918b193d8ddc2b76543d201cfd249"},
+    ("bwd_dkdv_kernel", "causal"): {"sources": {"fa_bwd.cu": _BWD}, "bytes": 372.54e6},
+    # the four-shard step: four forward launches over the key shards and the combine, summed
+    ("causal_sharded4", "causal"): {"sources": {"fa_fwd.cu": _FWD, "fa_decode.cu": _DEC}, "bytes": 1224.08e6},
     # decode: captured on the B4 slice (decode_small) and scaled by 16 to B64 (K/V streamed once)
-    ("decode_split_kernel", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2151.001e6,
-                                        "sha256": "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"},
-    ("decode_split_kernel_paged", "decode"): {"source": "fa_decode.cu", "bytes": 16 * 2150.928e6,
-                                              "sha256": "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"},
+    ("decode_split_kernel", "decode"): {"sources": {"fa_decode.cu": _DEC}, "bytes": 16 * 2151.001e6},
+    ("decode_split_kernel_paged", "decode"): {"sources": {"fa_decode.cu": _DEC}, "bytes": 16 * 2150.928e6},
 }
+
+
+def _traffic(kernel: str, workload: str):
+    rec = NCU_TRAFFIC.get((kernel, workload))
+    if rec is None:
+        return None
+    for src, sha in rec["sources"].items():
+        try:
+            with open(os.path.join(ROOT, "exact_attention_06_gb300", "csrc", src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != sha:
+                    return None
+        except OSError:
+            return None
+    return rec["bytes"]
 
 
 def _workload_label(w):
@@ -98,21 +111,37 @@ def _headline_config(w, world):
             "l2": l2}
 
 
-def _traffic(kernel: str, workload: str):
-    rec = NCU_TRAFFIC.get((kernel, workload))
-    if rec is None:
-        return None
-    try:
-        with open(os.path.join(ROOT, "exact_attention_06_gb300", "csrc", rec["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
-                return None
-    except OSError:
-        return None
-    return rec["bytes"]
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, clock event reasons)."""
+
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        c = self.c
+        mhz, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(mhz)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, c.byref(mx))
+        self.reasons_fn(self.h, c.byref(rs))
+        return float(mhz.value), float(mx.value), [n for b, n in self.REASONS.items() if rs.value & b]
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while a region runs."""
+    """SM clock and throttle reasons while a region runs: NVML polled every ~2 ms when the library
+    loads (enough samples for a timed region of tens of milliseconds), else nvidia-smi samples."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -126,6 +155,15 @@ class ClockSampler:
 
     def start(self):
         try:
+            self.nvml = _Nvml(self.device_index)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.stop_flag = False
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
+        try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "20"],
@@ -135,6 +173,18 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+
+    def _poll(self):
+        while not self.stop_flag:
+            smp = self.nvml.sample()
+            if smp is not None:
+                mhz, mx, reasons = smp
+                parts = ["", str(mhz), str(mx), ""] + ["" for _ in range(5)]
+                for i, name in enumerate(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                          "sw_power_cap")):
+                    parts[5 + i] = "Active" if name in reasons else "Not Active"
+                self.samples.append((time.time(), parts))
+            time.sleep(0.002)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -146,6 +196,9 @@ class ClockSampler:
         setattr(self, which, time.time())
 
     def stop(self):
+        if getattr(self, "nvml", None) is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -177,7 +230,8 @@ class ClockSampler:
                 if val.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+                "reasons": sorted(reasons), "samples": len(inside), "window": window,
+                "source": "nvml" if getattr(self, "nvml", None) is not None else "nvidia-smi"}
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:
@@ -550,9 +604,9 @@ def run_ours(args):
             "ms_per_step": round(stt, 4), "steps": args.extra_steps, "gpu_launches": nl * args.extra_steps,
             "config": {"B": wb.B, "H": wb.H, "N": wb.N, "d": wb.d, "causal": True, "shards": 4,
                        "spike_every_64th_key_x8": True},
-            "roofline": _roofline("tensor", wb.flops(), stt, peaks, None),
+            "roofline": _roofline("tensor", wb.flops(), stt, peaks, _traffic("causal_sharded4", "causal")),
             "note": "4 x fa_fwd_partial (one per 2048-key shard, concurrent streams) + fa_combine; "
-                    "flops of the unsharded forward"}
+                    "flops of the unsharded forward; traffic the DRAM bytes of the step's five launches"}
         del sst
         torch.cuda.empty_cache()
         # FP8 forward on the causal workload (E4M3 inputs with per-128-row block scales)

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dk,
                     void* __restrict__ dv, int N, float sl2, float scale, int grad_fp32,
                     unsigned long long budget, const __grid_constant__ CUtensorMap tdk,
-                    const __grid_constant__ CUtensorMap tdv) {
+                    const __grid_constant__ CUtensorMap tdv, int ng) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -268,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int kt = blockIdx.y;  // key tile; small kt has the most causal work and is scheduled first
+  int bh, kt;  // key tile; small kt has the most causal work and is scheduled first (within a head group)
+  grouped_block(ng, bh, kt);
   const int n_tiles = (N + kTile - 1) / kTile;
   const int i0 = CAUSAL ? kt : 0;  // first query tile that sees this key tile
   const int n_i = n_tiles - i0;
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dq, int N,
                   float sl2, float scale, int grad_fp32, unsigned long long budget,
-                  const __grid_constant__ CUtensorMap tdq) {
+                  const __grid_constant__ CUtensorMap tdq, int ng) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -573,9 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define BAR(i) (sBar + 8u * static_cast<uint32_t>(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  int bh, qt;
+  grouped_block(ng, bh, qt);
   const int n_tiles = (N + kTile - 1) / kTile;
-  const int qt = n_tiles - 1 - static_cast<int>(blockIdx.y);  // most causal work first
+  qt = n_tiles - 1 - qt;  // most causal work first (within a head group)
   const int n_j = CAUSAL ? qt + 1 : n_tiles;
 
   if (threadIdx.x == 0) {
@@ -743,18 +744,19 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
+  const int ng = head_groups(a.BH, n_tiles, CAUSAL, a.sms);
   dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_tiles));
   auto k1 = bwd_dkdv_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM)) != cudaSuccess)
     return e;
   k1<<<grid, kThreads, DkdvCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dk, a.dv, a.N,
-                                                   a.scale_log2, a.scale, a.grad_fp32, a.budget, a.tdk, a.tdv);
+                                                   a.scale_log2, a.scale, a.grad_fp32, a.budget, a.tdk, a.tdv, ng);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto k2 = bwd_dq_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM)) != cudaSuccess)
     return e;
   k2<<<grid, kThreads, DqCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dq, a.N, a.scale_log2,
-                                                 a.scale, a.grad_fp32, a.budget, a.tdq);
+                                                 a.scale, a.grad_fp32, a.budget, a.tdq, ng);
   return cudaGetLastError();
 }
 

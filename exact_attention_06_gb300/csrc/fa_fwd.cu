@@ -296,8 +296,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_launch();  // a dependent kernel may launch once every CTA has started
-  const int bh = blockIdx.x;
-  const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest causal work first
+  // Heads in aux.ng groups, the longest causal blocks of a group first: the blocks of a head read
+  // its K/V prefixes close together in time, from L2.
+  int bh, pair;
+  grouped_block(aux.ng, bh, pair);
+  pair = static_cast<int>(gridDim.y) - 1 - pair;
   const int n_tiles = (Nk + kBc - 1) / kBc;
   // KV steps of each query tile: all key tiles, or (causal) those holding a key at or before
   // its last row; 0 if the tile is past N.
@@ -1146,6 +1149,7 @@ cudaError_t launch_t(const FwdLaunch& a, cudaStream_t stream) {
   } else {
     // one CTA per block of 256 query rows (a split last round is planned for the persistent kernel only)
     if (aux.lin) return cudaErrorInvalidValue;
+    aux.ng = head_groups(a.BH, n_pairs, CAUSAL, a.sms);
     const dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_pairs));
     return launch_kernel(fwd_kernel<D, CAUSAL, FP8>, grid, C::THREADS, C::SMEM, stream, a.tq, a.tk, a.tv, a.o, a.lse,
                          a.N, a.scale_log2, a.o_fp32, a.budget, aux, a.to);

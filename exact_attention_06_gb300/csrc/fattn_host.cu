@@ -427,10 +427,12 @@ fa_status_t fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const flo
   const long long bh = static_cast<long long>(B) * H;
   if (bh > INT_MAX) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld exceeds the grid limit", bh);
   if ((N + 127) / 128 > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the 65535 query-tile grid limit", N);
-  fa_status_t st = check_device(nullptr);
+  int sms = 0;
+  fa_status_t st = check_device(&sms);
   if (st != FA_OK) return st;
 
   fattn::FwdLaunch a{};
+  a.sms = sms;
   if ((st = make_map(&a.tq, q8, d, N, bh, 128, 1)) != FA_OK) return st;
   if ((st = make_map(&a.tk, k8, d, N, bh, 128, 1)) != FA_OK) return st;
   if ((st = make_map(&a.tv, v8, d, N, bh, 128, 1)) != FA_OK) return st;
@@ -709,9 +711,11 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (!workspace || ws_bytes < need)
     return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
   if (!aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  fa_status_t st = check_device(nullptr);
+  int sms = 0;
+  fa_status_t st = check_device(&sms);
   if (st != FA_OK) return st;
   fattn::BwdLaunch a{};
+  a.sms = sms;
   if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tk, k, d, N, bh, 128)) != FA_OK) return st;
   if ((st = make_map(&a.tv, v, d, N, bh, 128)) != FA_OK) return st;

@@ -43,7 +43,23 @@ struct FwdAux {
   int qsplit;
   // Persistent CTAs (non-causal bf16 d = 64): the number of work items; set by launch_fwd.
   int n_items;
+  // One-block-per-CTA kernel: the heads are dispatched in ng groups (each group's blocks
+  // longest first) so that the blocks of a head run close together in time; set by launch_fwd.
+  int ng;
 };
+
+// Number of head groups for a grid (B*H, P) whose CTAs are ordered by grouped_block.  Causal:
+// every group needs enough heads that its work, spread over the SMs, outlasts its longest block
+// (about 2P tile steps against P^2 + P per head), or that block runs alone at the end of the
+// launch: at least 2 * sms / (P + 1) heads per group.  Non-causal blocks are all alike: about one
+// wave of CTAs per group.  Groups of near-equal size, so that no small group is left over.
+inline int head_groups(int bh, int n_ranks, bool causal, int sms) {
+  if (sms < 1 || n_ranks < 1 || bh < 1) return 1;
+  long long min_heads = causal ? (2LL * sms + n_ranks) / (n_ranks + 1) : (sms + n_ranks - 1) / n_ranks;
+  if (min_heads < 1) min_heads = 1;
+  const long long ng = bh / min_heads;
+  return static_cast<int>(ng < 1 ? 1 : ng);
+}
 
 struct FwdLaunch {
   CUtensorMap tq, tk, tv;
@@ -114,6 +130,7 @@ struct BwdLaunch {
   float scale;
   float scale_log2;
   unsigned long long budget;
+  int sms;  // SMs of the device (block order of the dK/dV and dQ kernels)
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
 unsigned int bwd_read_and_clear_status();

@@ -67,6 +67,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ---------------------------------------------------------------- block order
+// For a grid (B*H, P) of CTAs dispatched in linear order: the (head, work rank) of this CTA when
+// the heads are cut into ng groups of near-equal size (the first B*H mod ng groups one head
+// larger) and, within a group, rank 0 (the most work) of every head comes first, then rank 1, and
+// so on.  The blocks of a head then run close together in time and share its operands through
+// L2, while every group, the last included, ends on the blocks with the least work.
+__device__ __forceinline__ void grouped_block(int ng, int& bh, int& rank) {
+  const long long n_bh = gridDim.x, n_r = gridDim.y;
+  const long long l = static_cast<long long>(blockIdx.y) * n_bh + blockIdx.x;
+  const long long q = n_bh / ng, r = n_bh % ng;  // r groups of q + 1 heads, then ng - r of q
+  const long long big = r * (q + 1) * n_r;        // CTAs in the larger groups
+  long long g0, gs, i;
+  if (l < big) {
+    gs = q + 1;
+    g0 = (l / (gs * n_r)) * gs;
+    i = l - g0 * n_r;
+  } else {
+    gs = q;
+    const long long l2 = l - big;
+    g0 = r * (q + 1) + (l2 / (gs * n_r)) * gs;
+    i = l2 - (g0 - r * (q + 1)) * n_r;
+  }
+  rank = static_cast<int>(i / gs);
+  bh = static_cast<int>(g0 + i % gs);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

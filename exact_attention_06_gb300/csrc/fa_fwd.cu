@@ -313,6 +313,20 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   };
   const int n_t0 = steps_of(0), n_t1 = steps_of(1);
   const int n_max = max(n_t0, n_t1);
+  if (aux.u_part && n_max == 0) {
+    // A key shard that starts after every row of this block: each of the block's rows gets the
+    // empty partial (m = -inf, l = 0; U is never read for it), without setting up the pipeline.
+    grid_dep_wait();
+    for (int i = threadIdx.x; i < kRowsPerCta; i += blockDim.x) {
+      const int row = pair * kRowsPerCta + i;
+      if (row < N) {
+        const size_t slot = (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard;
+        aux.m_part[slot] = -INFINITY;
+        aux.l_part[slot] = 0.f;
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);

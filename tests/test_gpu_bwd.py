@@ -110,3 +110,22 @@ def test_backward_full_causal_size_sampled_rows_against_the_oracle():
         for fp32, (dq, dk, dv) in grads.items():
             got = (dq[b, h].index_select(0, qi), dk[b, h].index_select(0, ki), dv[b, h].index_select(0, ki))
             assert_grads(got, (dq_ref, dk_ref, dv_ref), f"full causal b={b} h={h} grad_fp32={fp32}")
+
+
+def test_backward_uneven_head_groups():
+    """37 heads of N = 2048, causal: the key (query) tiles are dispatched in head groups of unequal
+    size; dQ, dK, dV of heads in different groups against the row-restricted oracle."""
+    B, H, N, d = 1, 37, 2048, 128
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=73, device=DEV)
+    do = inputs.normal_bf16((B, H, N, d), seed=74, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    got = run_bwd(q, k, v, do, scale, True)
+    edge = [0, 127, 128, N - 1]
+    for h in (0, 18, 19, 36):
+        qr = np.unique(np.concatenate([inputs.sample_rows(N, 24, seed=h).numpy(), edge]))
+        kr = np.unique(np.concatenate([inputs.sample_rows(N, 24, seed=100 + h).numpy(), edge]))
+        ref = oracle.attention_backward_rows(q[0, h].cpu(), k[0, h].cpu(), v[0, h].cpu(), do[0, h].cpu(), scale,
+                                             True, q_rows=qr, k_rows=kr)
+        qi, ki = torch.from_numpy(qr).to(DEV), torch.from_numpy(kr).to(DEV)
+        g = (got[0][0, h].index_select(0, qi), got[1][0, h].index_select(0, ki), got[2][0, h].index_select(0, ki))
+        assert_grads(g, ref, f"37 heads h={h}")

@@ -137,3 +137,18 @@ def test_long_causal_configs_sampled_rows(name):
     for o_fp32 in (True, False):
         o, lse = run_fwd(q, k, v, w.scale, w.causal, o_fp32=o_fp32)
         assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref, f"{name} o_fp32={o_fp32}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_uneven_head_groups_cover_every_block(causal):
+    """37 heads of N = 4096: the block order cuts them into head groups of unequal size (19 + 18
+    causal, 13 + 12 + 12 non-causal); every block of every head is computed once and right."""
+    B, H, N, d = 1, 37, 4096, 128
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=37, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    rows = inputs.sample_rows_per_head(B, H, N, 12, seed=6)
+    edge = torch.tensor([0, 255, 256, N - 257, N - 1])
+    rows = torch.sort(torch.cat([rows, edge.expand(B, H, -1)], dim=2), dim=2).values
+    o_ref, lse_ref = _oracle(q, k, v, scale, causal, rows=rows.numpy())
+    o, lse = run_fwd(q, k, v, scale, causal, o_fp32=True)
+    assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref, f"37 heads causal={causal}")

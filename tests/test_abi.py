@@ -108,6 +108,27 @@ def test_decode_and_combine_argument_checks_need_no_gpu(lib):
     assert st == fattn.FA_ERR_UNSUPPORTED
 
 
+def test_decode_and_combine_options_are_checked_before_any_launch(lib):
+    """The _ex entry points reject a bad o_fp32 flag (and everything the plain calls reject)
+    before touching a GPU; a NULL options pointer means the defaults."""
+    from exact_attention_06_gb300 import fattn
+    vp, f, sz = ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+    bad = fattn.FaDecodeOpts(2, 0)
+    st = lib.fa_decode_splitkv_ex(vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, 256, 128, f(0.1), 128, 1, vp(256),
+                                  sz(1 << 20), vp(0), ctypes.byref(bad))
+    assert st == fattn.FA_ERR_INVALID_ARG and "o_fp32" in fattn.fa_last_error()
+    st = lib.fa_decode_splitkv_ex(vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, 256, 128, f(0.1), 128, 1, vp(256),
+                                  sz(16), vp(0), None)
+    assert st == fattn.FA_ERR_WORKSPACE
+    st = lib.fa_decode_paged_ex(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, 128, 64, 4, 4, 256,
+                                f(0.1), 0, vp(256), sz(1 << 20), vp(0), ctypes.byref(bad))
+    assert st == fattn.FA_ERR_INVALID_ARG and "o_fp32" in fattn.fa_last_error()
+    assert lib.fa_combine_ex(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 2, 128, 2, vp(0)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_combine_ex(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 0, 128, 1, vp(0)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_combine_ex(vp(16), vp(16), vp(16), vp(8), vp(16), 4, 2, 128, 1, vp(0)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_combine_ex(vp(16), vp(16), vp(16), vp(16), vp(16), 4, 2, 96, 0, vp(0)) == fattn.FA_ERR_UNSUPPORTED
+
+
 def test_fp8_argument_checks_need_no_gpu(lib):
     from exact_attention_06_gb300 import fattn
     vp, f = ctypes.c_void_p, ctypes.c_float

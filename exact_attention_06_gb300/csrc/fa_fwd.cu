@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           break;
         mbar_arrive_expect_tx(BAR(C::B_KF + ks), C::KVB);
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sK + ks * C::KVB + h * kBox, &tk, BAR(C::B_KF + ks), h * C::BOX_X, j * kBc, bh);
+          tma_load_3d(sK + ks * C::KVB + h * kBox, &tk, BAR(C::B_KF + ks), h * C::BOX_X, aux.kload0 + j * kBc, bh);
         k_issued = j + 1;
         const int vs = j % C::VST;
         if (j >= C::VST &&
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           break;
         mbar_arrive_expect_tx(BAR(C::B_VF + vs), C::KVB);
         for (int h = 0; h < C::NH; ++h)
-          tma_load_3d(sV + vs * C::KVB + h * kBox, &tv, BAR(C::B_VF + vs), h * C::BOX_X, j * kBc, bh);
+          tma_load_3d(sV + vs * C::KVB + h * kBox, &tv, BAR(C::B_VF + vs), h * C::BOX_X, aux.kload0 + j * kBc, bh);
         v_issued = j + 1;
       }
       // Every copy this CTA started must land before its shared memory is released.
@@ -768,7 +768,7 @@ struct FwdItem {
 __device__ __forceinline__ FwdItem item_at(int w, const FwdAux& aux, int N) {
   FwdItem I;
   I.koff = aux.koff;
-  I.kload = 0;
+  I.kload = aux.kload0;
   I.Nk = aux.Nk;
   I.to_part = aux.u_part != nullptr && !aux.lin;
   I.srow0 = 0;
@@ -784,7 +784,8 @@ __device__ __forceinline__ FwdItem item_at(int w, const FwdAux& aux, int N) {
     const int piece = w - aux.n_full;
     u = aux.n_full + piece / aux.ksplit;
     I.sadd = piece % aux.ksplit;
-    I.koff = I.kload = I.sadd * aux.kchunk;
+    I.koff = I.sadd * aux.kchunk;
+    I.kload = aux.kload0 + I.koff;
     I.Nk = min(aux.kchunk, N - I.koff);
     I.to_part = true;
     I.srow0 = aux.prow0;

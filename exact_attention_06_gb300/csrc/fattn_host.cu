@@ -347,15 +347,18 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, stream, nullptr);
 }
 
-fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u_part, float* m_part,
-                           float* l_part, int B, int H, int N, int Nk, int key_offset, int d, float scale, int causal,
-                           int shard, int S, void* stream) {
+fa_status_t fa_fwd_partial_ex(const void* q, const void* k, const void* v, float* u_part, float* m_part,
+                              float* l_part, int B, int H, int N, int Nk, int key_offset, int kv_rows, int d,
+                              float scale, int causal, int shard, int S, void* stream) {
   g_last_error[0] = '\0';
   if (!q || !k || !v || !u_part || !m_part || !l_part) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
   if (B < 1 || H < 1 || N < 1 || Nk < 1)
     return fail(FA_ERR_INVALID_ARG, "B, H, N and Nk must be >= 1 (got %d, %d, %d, %d)", B, H, N, Nk);
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
   if (key_offset < 0) return fail(FA_ERR_INVALID_ARG, "key_offset=%d must be >= 0", key_offset);
+  if (kv_rows < 0 || (kv_rows > 0 && static_cast<long long>(key_offset) + Nk > kv_rows))
+    return fail(FA_ERR_INVALID_ARG, "kv_rows=%d must be 0 or >= key_offset + Nk = %lld", kv_rows,
+                static_cast<long long>(key_offset) + Nk);
   if (S < 1 || shard < 0 || shard >= S) return fail(FA_ERR_INVALID_ARG, "shard=%d must be in [0, S=%d)", shard, S);
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
@@ -371,8 +374,12 @@ fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u
   fattn::FwdLaunch a{};
   a.sms = sms;
   if ((st = make_map(&a.tq, q, d, N, bh, 128)) != FA_OK) return st;
-  if ((st = make_map(&a.tk, k, d, Nk, bh, 128)) != FA_OK) return st;
-  if ((st = make_map(&a.tv, v, d, Nk, bh, 128)) != FA_OK) return st;
+  // The shard's own buffers ([B, H, Nk, d]), or the whole key tensors ([B, H, kv_rows, d]) read
+  // from row key_offset on.
+  const int rows = kv_rows > 0 ? kv_rows : Nk;
+  if ((st = make_map(&a.tk, k, d, rows, bh, 128)) != FA_OK) return st;
+  if ((st = make_map(&a.tv, v, d, rows, bh, 128)) != FA_OK) return st;
+  a.aux.kload0 = kv_rows > 0 ? key_offset : 0;
   a.N = N;
   a.BH = static_cast<int>(bh);
   a.d = d;
@@ -390,6 +397,13 @@ fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u
   cudaError_t e = fattn::launch_fwd(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_partial launch");
   return FA_OK;
+}
+
+fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u_part, float* m_part,
+                           float* l_part, int B, int H, int N, int Nk, int key_offset, int d, float scale, int causal,
+                           int shard, int S, void* stream) {
+  return fa_fwd_partial_ex(q, k, v, u_part, m_part, l_part, B, H, N, Nk, key_offset, 0, d, scale, causal, shard, S,
+                           stream);
 }
 
 fa_status_t fa_quantize_e4m3(const void* x, void* codes, float* scales, int B, int H, int N, int d, void* stream) {

@@ -25,6 +25,7 @@ struct FwdAux {
   const float* sv;
   int Nk;           // keys of this launch (= N unless a key shard)
   int koff;         // global index of key 0 (causal masking of a key shard)
+  int kload0;       // row of the k, v tensors (as mapped) that holds key 0 of this launch
   float* u_part;    // key shard: partials [BH*N, S, d], [BH*N, S], [BH*N, S]; null = write O, lse
   float* m_part;
   float* l_part;

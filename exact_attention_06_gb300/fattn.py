@@ -25,7 +25,8 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 # Every symbol include/fattn.h declares.
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8",
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_fwd_partial", "fa_fwd_partial_ex",
+            "fa_quantize_e4m3", "fa_fwd_fp8",
             "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes", "fa_decode_splitkv",
             "fa_decode_splitkv_ex", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes",
             "fa_decode_paged", "fa_decode_paged_ex", "fa_combine", "fa_combine_ex", "fa_get_status",
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_workspace_bytes.argtypes = [i, i, i, i, i]
         L.fa_fwd_workspace_bytes.restype = sz
         L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp]
+        L.fa_fwd_partial_ex.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp]
         L.fa_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, i, vp]
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.POINTER(FaFwdOpts)]
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
@@ -87,7 +89,8 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_quantize_e4m3", "fa_fwd_fp8", "fa_bwd",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_fwd_partial_ex", "fa_quantize_e4m3", "fa_fwd_fp8",
+                     "fa_bwd",
                      "fa_decode_splitkv", "fa_decode_splitkv_ex", "fa_decode_splitkv_noalloc", "fa_decode_paged",
                      "fa_decode_paged_ex", "fa_combine", "fa_combine_ex", "fa_get_status"):
             getattr(L, name).restype = i
@@ -163,15 +166,19 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None):
 
 
 def fa_fwd_partial(q, k, v, u_part, m_part, l_part, scale: float, key_offset: int, shard: int,
-                   causal: bool = False, stream=None):
-    """Forward over one key shard: q [B, H, N, d]; k, v [B, H, Nk, d] (global key indices from
-    key_offset); writes slot ``shard`` of u_part [B*H*N, S, d], m_part / l_part [B*H*N, S] fp32."""
+                   causal: bool = False, stream=None, nk: int | None = None):
+    """Forward over one key shard: q [B, H, N, d]; writes slot ``shard`` of u_part [B*H*N, S, d],
+    m_part / l_part [B*H*N, S] fp32.  k, v are the shard's own [B, H, Nk, d] buffers (global key
+    indices from key_offset), or, with ``nk``, the whole [B, H, L, d] key tensors of which the
+    shard is rows key_offset .. key_offset + nk - 1 (fa_fwd_partial_ex, no copy)."""
     B, H, N, d = q.shape
-    Nk = k.shape[2]
     S = u_part.shape[1]
-    st = lib().fa_fwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(u_part), _ptr(m_part), _ptr(l_part), B, H, N, Nk,
-                              int(key_offset), d, float(scale), int(bool(causal)), int(shard), S, _stream(stream))
-    _check(st, "fa_fwd_partial")
+    kv_rows = 0 if nk is None else k.shape[2]
+    Nk = k.shape[2] if nk is None else int(nk)
+    st = lib().fa_fwd_partial_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(u_part), _ptr(m_part), _ptr(l_part), B, H, N, Nk,
+                                 int(key_offset), kv_rows, d, float(scale), int(bool(causal)), int(shard), S,
+                                 _stream(stream))
+    _check(st, "fa_fwd_partial_ex")
 
 
 def fa_quantize_e4m3(x, codes, scales, stream=None):

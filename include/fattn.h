@@ -136,6 +136,19 @@ fa_status_t fa_fwd_partial(const void* q, const void* k, const void* v, float* u
                            float* l_part, int B, int H, int N, int Nk, int key_offset, int d,
                            float scale, int causal, int shard, int S, void* stream);
 
+/* fa_fwd_partial reading the shard straight from the whole key tensors, with no per-shard copy:
+ *   k, v     [B, H, kv_rows, d] bf16, 16-byte aligned: the full key sequence of every head; the
+ *            shard is rows key_offset .. key_offset + Nk - 1 of each head (its global key
+ *            indices, as for fa_fwd_partial).  kv_rows >= key_offset + Nk.  Keys of the tensor
+ *            outside the shard may be read (a tile that ends inside the shard) and are masked
+ *            as inadmissible.
+ *   kv_rows  0: k, v are the shard's own [B, H, Nk, d] buffers, exactly fa_fwd_partial.
+ * Other arguments, results and errors as fa_fwd_partial (FA_ERR_INVALID_ARG for kv_rows < 0 or
+ * kv_rows < key_offset + Nk). */
+fa_status_t fa_fwd_partial_ex(const void* q, const void* k, const void* v, float* u_part, float* m_part,
+                              float* l_part, int B, int H, int N, int Nk, int key_offset, int kv_rows,
+                              int d, float scale, int causal, int shard, int S, void* stream);
+
 /*
  * fa_quantize_e4m3 -- block quantization of Q, K or V for fa_fwd_fp8
  * (triton-tutorial "8. FlashAttention 实战", §8.9.4: one scale per block of

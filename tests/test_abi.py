@@ -198,6 +198,20 @@ def test_partial_forward_argument_checks_need_no_gpu(lib):
     assert part(ptrs=(16, 16, 16, 16, 0, 16)) == fattn.FA_ERR_INVALID_ARG
 
 
+def test_partial_forward_key_range_checks_need_no_gpu(lib):
+    from exact_attention_06_gb300 import fattn
+    vp, f = ctypes.c_void_p, ctypes.c_float
+
+    def part(Nk=100, key_offset=200, kv_rows=300):
+        return lib.fa_fwd_partial_ex(*(vp(16) for _ in range(6)), 1, 1, 256, Nk, key_offset, kv_rows, 64, f(0.1), 1,
+                                     0, 2, vp(0))
+
+    assert part(kv_rows=299) == fattn.FA_ERR_INVALID_ARG  # the shard ends past the tensor
+    assert part(kv_rows=-1) == fattn.FA_ERR_INVALID_ARG
+    assert part(key_offset=-1) == fattn.FA_ERR_INVALID_ARG
+    assert "kv_rows" in fattn.fa_last_error() or "key_offset" in fattn.fa_last_error()
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     # no fallback: a missing libfattn.so is an error, not a silent CPU path
     from exact_attention_06_gb300 import fattn

@@ -21,10 +21,10 @@ def _built():
     ensure_built()
 
 
-def run_sharded(q, k, v, cuts, scale, causal, streams=False, o_fp32=False):
-    """One fa_fwd_partial per shard [cuts[s], cuts[s+1]) (each shard its own K/V buffers), then
-    fa_combine (fp32 or bf16 O); with ``streams`` every shard runs on its own stream.  Returns
-    (o [B,H,N,d], lse, u, m, l)."""
+def run_sharded(q, k, v, cuts, scale, causal, streams=False, o_fp32=False, views=False):
+    """One fa_fwd_partial per shard [cuts[s], cuts[s+1]) (each shard its own K/V buffers, or with
+    ``views`` the whole K/V tensors and the shard's key range), then fa_combine (fp32 or bf16 O);
+    with ``streams`` every shard runs on its own stream.  Returns (o [B,H,N,d], lse, u, m, l)."""
     B, H, N, d = q.shape
     S = len(cuts) - 1
     R = B * H * N
@@ -37,8 +37,12 @@ def run_sharded(q, k, v, cuts, scale, causal, streams=False, o_fp32=False):
     side = [torch.cuda.Stream() for _ in range(S)] if streams else [main] * S
     for s in range(S):
         side[s].wait_stream(main)
-        fattn.fa_fwd_partial(q, ks[s], vs[s], u, m, l, scale, key_offset=cuts[s], shard=s, causal=causal,
-                             stream=side[s])
+        if views:
+            fattn.fa_fwd_partial(q, k, v, u, m, l, scale, key_offset=cuts[s], shard=s, causal=causal, stream=side[s],
+                                 nk=cuts[s + 1] - cuts[s])
+        else:
+            fattn.fa_fwd_partial(q, ks[s], vs[s], u, m, l, scale, key_offset=cuts[s], shard=s, causal=causal,
+                                 stream=side[s])
         main.wait_stream(side[s])
     o = torch.empty((R, d), dtype=torch.float32 if o_fp32 else torch.bfloat16, device=DEV)
     lse = torch.empty(R, dtype=torch.float32, device=DEV)
@@ -122,3 +126,22 @@ def test_sharded_noncausal_d64_many_items_per_cta():
     # non-causal N=2048: every row averages 2048 keys, |O| is small and bf16 O meets the raw bounds
     assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref, "sharded d64 non-causal",
                   raw=True)
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (64, True), (128, False), (128, True)])
+def test_shards_read_from_the_whole_key_tensors(d, causal):
+    """fa_fwd_partial_ex on the whole K/V tensors (each shard a key range, no copy) gives the
+    partials of the per-shard buffers bit for bit, also where a shard's last key tile runs into
+    the next shard's keys (cuts off the 128-key grid), and the merged forward matches the oracle."""
+    B, H, N = 1, 3, 1000
+    cuts = [0, 300, 701, 1000]
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=d + 5, device=DEV)
+    scale = 1 / math.sqrt(d)
+    o1, lse1, u1, m1, l1 = run_sharded(q, k, v, cuts, scale, causal, o_fp32=True)
+    o2, lse2, u2, m2, l2 = run_sharded(q, k, v, cuts, scale, causal, o_fp32=True, views=True)
+    assert torch.equal(m1, m2) and torch.equal(l1, l2)
+    ne = ~torch.isneginf(m1)
+    assert torch.equal(u1[ne], u2[ne])  # an empty partial's U is never written
+    assert torch.equal(o1, o2) and torch.equal(lse1, lse2)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), scale, causal)
+    assert_parity(o2, lse2, o_ref, lse_ref, f"whole-tensor shards d={d} causal={causal}")

@@ -128,6 +128,28 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+_BF16 = (torch.bfloat16,)
+_F32 = (torch.float32,)
+_OUT = (torch.bfloat16, torch.float32)
+_U8 = (torch.uint8,)
+_I32 = (torch.int32,)
+
+
+def _need(func: str, name: str, t, dtypes, shape=None):
+    """The library reads and writes plain contiguous device buffers: refuse anything else here,
+    before a pointer is passed (a strided view or a host tensor would be read as garbage)."""
+    if not isinstance(t, torch.Tensor):
+        raise FattnError(FA_ERR_INVALID_ARG, func, f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise FattnError(FA_ERR_INVALID_ARG, func, f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise FattnError(FA_ERR_INVALID_ARG, func, f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise FattnError(FA_ERR_INVALID_ARG, func, f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise FattnError(FA_ERR_INVALID_ARG, func, f"{name} must be a CUDA tensor")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -147,8 +169,16 @@ def fa_fwd_ex(q, k, v, o, lse, scale: float, causal: bool = False, stream=None, 
     an optional uint8 CUDA tensor of at least fa_fwd_workspace_bytes() bytes for the key split.
     """
     B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need("fa_fwd_ex", name, t, _BF16, (B, H, N, d))
+    _need("fa_fwd_ex", "o", o, _OUT, (B, H, N, d))
+    _need("fa_fwd_ex", "lse", lse, _F32, (B, H, N))
+    if workspace is not None:
+        _need("fa_fwd_ex", "workspace", workspace, _U8)
     if o_fp32 is None:
         o_fp32 = o.dtype == torch.float32
+    elif bool(o_fp32) != (o.dtype == torch.float32):
+        raise FattnError(FA_ERR_INVALID_ARG, "fa_fwd_ex", f"o_fp32={o_fp32} but o has dtype {o.dtype}")
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     opts = FaFwdOpts(int(bool(o_fp32)), int(wait_budget_cycles), _ptr(workspace) if workspace is not None else None,
                      ws_bytes)
@@ -160,6 +190,9 @@ def fa_fwd_ex(q, k, v, o, lse, scale: float, causal: bool = False, stream=None, 
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None):
     """Fused forward with bf16 O (see fa_fwd_ex)."""
     B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need("fa_fwd", name, t, _BF16, (B, H, N, d))
+    _need("fa_fwd", "lse", lse, _F32, (B, H, N))
     st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
                       _stream(stream))
     _check(st, "fa_fwd")
@@ -172,7 +205,13 @@ def fa_fwd_partial(q, k, v, u_part, m_part, l_part, scale: float, key_offset: in
     indices from key_offset), or, with ``nk``, the whole [B, H, L, d] key tensors of which the
     shard is rows key_offset .. key_offset + nk - 1 (fa_fwd_partial_ex, no copy)."""
     B, H, N, d = q.shape
+    _need("fa_fwd_partial", "q", q, _BF16, (B, H, N, d))
+    _need("fa_fwd_partial", "k", k, _BF16, (B, H, k.shape[2], d))
+    _need("fa_fwd_partial", "v", v, _BF16, tuple(k.shape))
     S = u_part.shape[1]
+    _need("fa_fwd_partial", "u_part", u_part, _F32, (B * H * N, S, d))
+    _need("fa_fwd_partial", "m_part", m_part, _F32, (B * H * N, S))
+    _need("fa_fwd_partial", "l_part", l_part, _F32, (B * H * N, S))
     kv_rows = 0 if nk is None else k.shape[2]
     Nk = k.shape[2] if nk is None else int(nk)
     st = lib().fa_fwd_partial_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(u_part), _ptr(m_part), _ptr(l_part), B, H, N, Nk,
@@ -184,6 +223,9 @@ def fa_fwd_partial(q, k, v, u_part, m_part, l_part, scale: float, key_offset: in
 def fa_quantize_e4m3(x, codes, scales, stream=None):
     """E4M3 block quantization: x [B, H, N, d] bf16 -> codes [B, H, N, d] uint8, scales [B, H, ceil(N/128)] fp32."""
     B, H, N, d = x.shape
+    _need("fa_quantize_e4m3", "x", x, _BF16)
+    _need("fa_quantize_e4m3", "codes", codes, _U8, (B, H, N, d))
+    _need("fa_quantize_e4m3", "scales", scales, _F32, (B, H, (N + 127) // 128))
     st = lib().fa_quantize_e4m3(_ptr(x), _ptr(codes), _ptr(scales), B, H, N, d, _stream(stream))
     _check(st, "fa_quantize_e4m3")
 
@@ -193,6 +235,12 @@ def fa_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale: float, causal: bool = Fals
     """FP8 forward: q8, k8, v8 [B, H, N, 128] uint8 E4M3 codes with block scales sq, sk, sv
     [B, H, ceil(N/128)] fp32; o [B, H, N, 128] bf16 or fp32 (from its dtype); lse [B, H, N] fp32."""
     B, H, N, d = q8.shape
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        _need("fa_fwd_fp8", name, t, _U8, (B, H, N, d))
+    for name, t in (("sq", sq), ("sk", sk), ("sv", sv)):
+        _need("fa_fwd_fp8", name, t, _F32, (B, H, (N + 127) // 128))
+    _need("fa_fwd_fp8", "o", o, _OUT, (B, H, N, d))
+    _need("fa_fwd_fp8", "lse", lse, _F32, (B, H, N))
     opts = FaFwdOpts(int(o.dtype == torch.float32), int(wait_budget_cycles))
     st = lib().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse), B, H, N, d,
                           float(scale), int(bool(causal)), _stream(stream), ctypes.byref(opts))
@@ -206,8 +254,14 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool = False, workspace=None, stream=None):
     """Backward: gradients dq, dk, dv (bf16 or fp32, from dq's dtype) of the forward that produced o, lse."""
     B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need("fa_bwd", name, t, _BF16, (B, H, N, d))
+    _need("fa_bwd", "lse", lse, _F32, (B, H, N))
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need("fa_bwd", name, t, (dq.dtype,) if dq.dtype in _OUT else _OUT, (B, H, N, d))
     if workspace is None:
         workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N), dtype=torch.uint8, device=q.device)
+    _need("fa_bwd", "workspace", workspace, _U8)
     ws_bytes = workspace.numel() * workspace.element_size()
     grad_fp32 = int(dq.dtype == torch.float32)
     st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
@@ -224,6 +278,13 @@ def fa_decode_splitkv(q, k, v, o, lse, scale: float, workspace, chunk: int = 128
     """Split-KV decode: q [B, H, d], k/v [B, H, L, d], o [B, H, d] bf16 or fp32 (from its dtype),
     lse [B, H]; workspace a uint8 CUDA tensor (fa_decode_splitkv_ex)."""
     B, H, L, d = k.shape
+    _need("fa_decode_splitkv", "q", q, _BF16, (B, H, d))
+    _need("fa_decode_splitkv", "k", k, _BF16)
+    _need("fa_decode_splitkv", "v", v, _BF16, (B, H, L, d))
+    _need("fa_decode_splitkv", "o", o, _OUT, (B, H, d))
+    _need("fa_decode_splitkv", "lse", lse, _F32, (B, H))
+    if workspace is not None:
+        _need("fa_decode_splitkv", "workspace", workspace, _U8)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     opts = FaDecodeOpts(int(o.dtype == torch.float32), int(wait_budget_cycles))
     st = lib().fa_decode_splitkv_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale), chunk,
@@ -240,6 +301,11 @@ def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, chunk: int = 128, s
     GPU share that array and race: keep them on one stream.
     """
     B, H, L, d = k.shape
+    _need("fa_decode_splitkv_noalloc", "q", q, _BF16, (B, H, d))
+    _need("fa_decode_splitkv_noalloc", "k", k, _BF16)
+    _need("fa_decode_splitkv_noalloc", "v", v, _BF16, (B, H, L, d))
+    _need("fa_decode_splitkv_noalloc", "o", o, _BF16, (B, H, d))
+    _need("fa_decode_splitkv_noalloc", "lse", lse, _F32, (B, H))
     st = lib().fa_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, float(scale),
                                          chunk, splits, _stream(stream))
     _check(st, "fa_decode_splitkv_noalloc")
@@ -258,9 +324,17 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale: f
     B, H, d = q.shape
     P, _, page_size, _ = k_pages.shape
     max_pages = block_table.shape[1]
+    _need("fa_decode_paged", "q", q, _BF16, (B, H, d))
+    _need("fa_decode_paged", "k_pages", k_pages, _BF16, (P, H, page_size, d))
+    _need("fa_decode_paged", "v_pages", v_pages, _BF16, (P, H, page_size, d))
+    _need("fa_decode_paged", "block_table", block_table, _I32, (B, max_pages))
+    _need("fa_decode_paged", "seq_lens", seq_lens, _I32, (B,))
+    _need("fa_decode_paged", "o", o, _OUT, (B, H, d))
+    _need("fa_decode_paged", "lse", lse, _F32, (B, H))
     if workspace is None:
         workspace = torch.empty(fa_decode_paged_workspace_bytes(B, H, max_seq_len, d, page_size, max_pages, splits),
                                 dtype=torch.uint8, device=q.device)
+    _need("fa_decode_paged", "workspace", workspace, _U8)
     ws_bytes = workspace.numel() * workspace.element_size()
     opts = FaDecodeOpts(int(o.dtype == torch.float32), int(wait_budget_cycles))
     st = lib().fa_decode_paged_ex(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o),
@@ -273,6 +347,11 @@ def fa_combine(u_part, m_part, l_part, o, lse, stream=None):
     """Merge partials: u_part [R, S, d], m_part/l_part [R, S] fp32 -> o [R, d] bf16 or fp32 (from its
     dtype; fa_combine_ex), lse [R] fp32."""
     R, S, d = u_part.shape
+    _need("fa_combine", "u_part", u_part, _F32, (R, S, d))
+    _need("fa_combine", "m_part", m_part, _F32, (R, S))
+    _need("fa_combine", "l_part", l_part, _F32, (R, S))
+    _need("fa_combine", "o", o, _OUT, (R, d))
+    _need("fa_combine", "lse", lse, _F32, (R,))
     st = lib().fa_combine_ex(_ptr(u_part), _ptr(m_part), _ptr(l_part), _ptr(o), _ptr(lse), R, S, d,
                              int(o.dtype == torch.float32), _stream(stream))
     _check(st, "fa_combine_ex")

@@ -220,3 +220,38 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     with pytest.raises(fattn.FattnError) as ei:
         fattn.lib()
     assert "missing" in str(ei.value)
+
+
+def test_binding_rejects_tensors_the_library_cannot_read(lib):
+    """The binding passes raw device pointers, so it refuses host tensors, strided views, wrong
+    dtypes and mismatched shapes with FA_ERR_INVALID_ARG before anything reaches the library."""
+    import torch
+    from exact_attention_06_gb300 import fattn
+    B, H, N, d = 1, 2, 16, 64
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    lse = torch.zeros(B, H, N, dtype=torch.float32)
+
+    def rejected(fn, *args, what, **kw):
+        with pytest.raises(fattn.FattnError) as err:
+            fn(*args, **kw)
+        assert err.value.status == fattn.FA_ERR_INVALID_ARG
+        assert what in str(err.value), str(err.value)
+
+    # (the checks run in argument order and each tensor is checked for dtype, shape, layout and
+    # device in turn; the tensors here are on the host, so the faulty one goes first)
+    rejected(fattn.fa_fwd, q, q, q, q, lse, 0.1, what="CUDA tensor")
+    rejected(fattn.fa_fwd, q.transpose(2, 3).contiguous().transpose(2, 3), q, q, q, lse, 0.1, what="contiguous")
+    rejected(fattn.fa_fwd, q.float(), q, q, q, lse, 0.1, what="dtype")
+    k = torch.zeros(B, H, N // 2, d, dtype=torch.bfloat16)
+    rejected(fattn.fa_fwd_partial, q.float(), k, k, torch.zeros(B * H * N, 2, d), torch.zeros(B * H * N, 2),
+             torch.zeros(B * H * N, 2), 0.1, 0, 0, what="dtype")
+    rejected(fattn.fa_decode_splitkv, q[:, :, 0], q, q, q[:, :, 0].contiguous(), lse[:, :, 0].contiguous(), 0.1,
+             torch.zeros(256, dtype=torch.uint8), what="q must be contiguous")
+    u = torch.zeros(4, 2, d)
+    m = torch.zeros(4, 2)
+    rejected(fattn.fa_combine, u.double(), m, m, torch.zeros(4, d), torch.zeros(4), what="u_part")
+    rejected(fattn.fa_decode_splitkv, q[:, :1, 0].contiguous(), q, q, q[:, :, 0].contiguous(),
+             lse[:, :, 0].contiguous(), 0.1, torch.zeros(256, dtype=torch.uint8), what="shape")
+    rejected(fattn.fa_decode_paged, q[:, :, 0].contiguous().float(), q, q, torch.zeros(1, 4, dtype=torch.int32),
+             torch.zeros(1, dtype=torch.int32), q[:, :, 0].contiguous(), lse[:, :, 0].contiguous(), 0.1, 64,
+             workspace=torch.zeros(256, dtype=torch.uint8), what="dtype")

@@ -707,6 +707,13 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N) {
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int grad_fp32,
                    void* workspace, size_t ws_bytes, void* stream) {
+  return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, grad_fp32, workspace, ws_bytes,
+                   stream, nullptr);
+}
+
+fa_status_t fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int grad_fp32,
+                      void* workspace, size_t ws_bytes, void* stream, const fa_bwd_opts* opts) {
   g_last_error[0] = '\0';
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
   if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H and N must be >= 1 (got %d, %d, %d)", B, H, N);
@@ -753,7 +760,7 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   a.grad_fp32 = grad_fp32;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.budget = kDefaultBudget;
+  a.budget = (opts && opts->wait_budget_cycles) ? opts->wait_budget_cycles : kDefaultBudget;
   cudaGetLastError();
   cudaError_t e = fattn::launch_bwd(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");

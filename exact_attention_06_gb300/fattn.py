@@ -27,7 +27,7 @@ FA_ERR_WORKSPACE = 6
 # Every symbol include/fattn.h declares.
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_fwd_partial", "fa_fwd_partial_ex",
             "fa_quantize_e4m3", "fa_fwd_fp8",
-            "fa_bwd_workspace_bytes", "fa_bwd", "fa_decode_workspace_bytes", "fa_decode_splitkv",
+            "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_decode_workspace_bytes", "fa_decode_splitkv",
             "fa_decode_splitkv_ex", "fa_decode_splitkv_noalloc", "fa_decode_paged_workspace_bytes",
             "fa_decode_paged", "fa_decode_paged_ex", "fa_combine", "fa_combine_ex", "fa_get_status",
             "fa_status_string", "fa_last_error")
@@ -47,6 +47,10 @@ class FaFwdOpts(ctypes.Structure):
 
 class FaDecodeOpts(ctypes.Structure):
     _fields_ = [("o_fp32", ctypes.c_int), ("wait_budget_cycles", ctypes.c_ulonglong)]
+
+
+class FaBwdOpts(ctypes.Structure):
+    _fields_ = [("wait_budget_cycles", ctypes.c_ulonglong)]
 
 
 _lib = None
@@ -71,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
         L.fa_bwd_workspace_bytes.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+        L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp,
+                                ctypes.POINTER(FaBwdOpts)]
         L.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.fa_decode_workspace_bytes.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
@@ -90,7 +96,7 @@ def lib() -> ctypes.CDLL:
         L.fa_last_error.argtypes = []
         L.fa_last_error.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_partial", "fa_fwd_partial_ex", "fa_quantize_e4m3", "fa_fwd_fp8",
-                     "fa_bwd",
+                     "fa_bwd", "fa_bwd_ex",
                      "fa_decode_splitkv", "fa_decode_splitkv_ex", "fa_decode_splitkv_noalloc", "fa_decode_paged",
                      "fa_decode_paged_ex", "fa_combine", "fa_combine_ex", "fa_get_status"):
             getattr(L, name).restype = i
@@ -251,8 +257,10 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
     return int(lib().fa_bwd_workspace_bytes(B, H, N))
 
 
-def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool = False, workspace=None, stream=None):
-    """Backward: gradients dq, dk, dv (bf16 or fp32, from dq's dtype) of the forward that produced o, lse."""
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool = False, workspace=None, stream=None,
+           wait_budget_cycles: int = 0):
+    """Backward: gradients dq, dk, dv (bf16 or fp32, from dq's dtype) of the forward that produced o, lse.
+    A non-zero wait_budget_cycles calls fa_bwd_ex with that per-wait budget."""
     B, H, N, d = q.shape
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _need("fa_bwd", name, t, _BF16, (B, H, N, d))
@@ -264,9 +272,13 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool = False
     _need("fa_bwd", "workspace", workspace, _U8)
     ws_bytes = workspace.numel() * workspace.element_size()
     grad_fp32 = int(dq.dtype == torch.float32)
-    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H,
-                      N, d, float(scale), int(bool(causal)), grad_fp32, _ptr(workspace), ws_bytes, _stream(stream))
-    _check(st, "fa_bwd")
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+            float(scale), int(bool(causal)), grad_fp32, _ptr(workspace), ws_bytes, _stream(stream))
+    if wait_budget_cycles:
+        opts = FaBwdOpts(int(wait_budget_cycles))
+        _check(lib().fa_bwd_ex(*args, ctypes.byref(opts)), "fa_bwd_ex")
+    else:
+        _check(lib().fa_bwd(*args), "fa_bwd")
 
 
 def fa_decode_workspace_bytes(B: int, H: int, L: int, d: int, chunk: int = 128, splits: int = 0) -> int:

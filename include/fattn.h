@@ -363,7 +363,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N);
  * (triton-tutorial "8. FlashAttention 实战", §8.8.1-§8.8.4; operatorworld,
  * "反向传播：用重算换显存").  P is never stored: one kernel owns a key tile
  * and produces its dK, dV; another owns a query tile and produces its dQ
- * (no atomics).
+ * (no atomics: every output is written by one CTA in a fixed order, so the
+ * gradients are bitwise repeatable).
  *
  *   q, k, v, o, dout  [B, H, N, d] bf16, 16-byte aligned; o and lse must be the
  *                     forward's outputs for the same q, k, v, scale, causal.
@@ -379,6 +380,21 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                    float scale, int causal, int grad_fp32, void* workspace, size_t ws_bytes,
                    void* stream);
+
+/* Options of fa_bwd_ex.  wait_budget_cycles: per-wait budget in SM cycles of
+ * the dK/dV and dQ kernels, as in fa_fwd_opts (0 = the default, about 2 s);
+ * a wait that runs out ends the kernel, and fa_get_status then reports
+ * FA_ERR_TIMEOUT (the gradients are undefined). */
+typedef struct fa_bwd_opts {
+  unsigned long long wait_budget_cycles;
+} fa_bwd_opts;
+
+/* fa_bwd with options; opts may be NULL (then it is fa_bwd).  Arguments,
+ * results and errors otherwise as fa_bwd. */
+fa_status_t fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                      float scale, int causal, int grad_fp32, void* workspace, size_t ws_bytes,
+                      void* stream, const fa_bwd_opts* opts);
 
 /*
  * fa_get_status -- synchronise `stream`, then read and clear the current

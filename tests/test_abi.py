@@ -79,6 +79,27 @@ def test_forward_workspace_query_without_a_split(lib):
     assert lib.fa_fwd_workspace_bytes(4, 16, 2048, 64, 1) == 0
 
 
+def test_backward_workspace_and_options_need_no_gpu(lib):
+    """fa_bwd_workspace_bytes is D's size (B*H*N fp32, 256-byte rounded); fa_bwd_ex with options
+    and fa_bwd reject a too small workspace and an unsupported d before any device call."""
+    from exact_attention_06_gb300 import fattn
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    assert fattn.fa_bwd_workspace_bytes(2, 16, 8192) == 2 * 16 * 8192 * 4
+    assert fattn.fa_bwd_workspace_bytes(1, 1, 3) == 256
+    assert fattn.fa_bwd_workspace_bytes(0, 1, 3) == 0
+    need = fattn.fa_bwd_workspace_bytes(1, 1, 256)
+    ptrs = [vp(256)] * 9
+    opts = fattn.FaBwdOpts(1000)
+
+    def bwd_ex(ws_bytes, d=128, o=ctypes.byref(opts)):
+        return lib.fa_bwd_ex(*ptrs, 1, 1, 256, d, f(0.1), 1, 0, vp(256), ws_bytes, vp(0), o)
+
+    assert bwd_ex(need - 1) == fattn.FA_ERR_WORKSPACE
+    assert bwd_ex(need - 1, o=None) == fattn.FA_ERR_WORKSPACE
+    assert bwd_ex(need, d=96) == fattn.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd(*ptrs, 1, 1, 256, 128, f(0.1), 1, 0, vp(256), need - 1, vp(0)) == fattn.FA_ERR_WORKSPACE
+
+
 def test_decode_workspace_sizes(lib):
     from exact_attention_06_gb300 import fattn
     # explicit splits need no device: R*S*d floats + R*S + R*S floats, each rounded up to 256 bytes

@@ -36,7 +36,7 @@ def run_bwd(q, k, v, do, scale, causal, grad_fp32=True):
     dt = torch.float32 if grad_fp32 else torch.bfloat16
     dq, dk, dv = (torch.full((B, H, N, d), float("nan"), dtype=dt, device=DEV) for _ in range(3))
     fattn.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal)
-    fattn.fa_get_status()
+    assert fattn.fa_get_status() == fattn.FA_OK
     return dq, dk, dv
 
 

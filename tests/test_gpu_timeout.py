@@ -86,3 +86,30 @@ def test_decode_wait_budget_expiry_is_reported_and_the_context_survives(paged):
     assert fattn.fa_get_status() == fattn.FA_OK
     o_ref, lse_ref = oracle.decode(q.cpu(), k.cpu(), v.cpu(), scale)
     assert_parity(o2.reshape(B * H, d), lse2.reshape(B * H), o_ref, lse_ref, f"decode after a timeout paged={paged}")
+
+
+
+def test_backward_wait_budget_expiry_is_reported_and_the_context_survives():
+    """fa_bwd_ex with a one-cycle budget: the dK/dV and dQ kernels give up at their first waits,
+    drain their copies and MMAs, report FA_ERR_TIMEOUT, and the next backward on the same
+    context matches the oracle."""
+    ensure_built()
+    B, H, N, d = 1, 3, 700, 128
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=41, device=DEV)
+    do = inputs.normal_bf16((B, H, N, d), seed=42, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, scale, True)
+    grads = [torch.zeros(B, H, N, d, dtype=torch.float32, device=DEV) for _ in range(3)]
+    fattn.fa_bwd(q, k, v, o, do, lse, *grads, scale, True, wait_budget_cycles=1)
+    with pytest.raises(fattn.FattnError) as err:
+        fattn.fa_get_status()
+    assert err.value.status == fattn.FA_ERR_TIMEOUT
+    assert fattn.fa_get_status() == fattn.FA_OK
+    grads = [torch.full((B, H, N, d), float("nan"), dtype=torch.float32, device=DEV) for _ in range(3)]
+    fattn.fa_bwd(q, k, v, o, do, lse, *grads, scale, True)
+    assert fattn.fa_get_status() == fattn.FA_OK
+    ref = oracle.attention_backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), scale, True)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        e = g.double().cpu().numpy() - r
+        assert abs(e).max() <= 2e-2 * abs(r).max(), f"{name} after a timeout"
+        assert abs(e).mean() <= 1e-2 * abs(r).mean(), f"{name} after a timeout"

@@ -129,3 +129,25 @@ def test_backward_uneven_head_groups():
         qi, ki = torch.from_numpy(qr).to(DEV), torch.from_numpy(kr).to(DEV)
         g = (got[0][0, h].index_select(0, qi), got[1][0, h].index_select(0, ki), got[2][0, h].index_select(0, ki))
         assert_grads(g, ref, f"37 heads h={h}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_d64_long_sampled_rows(causal):
+    """d = 64 (the dK/dV kernel in two 64-query halves per query tile) over N = 4093 with x8 key
+    spikes and a ragged last tile: dQ at seeded query rows and dK, dV at seeded key rows (plus
+    tile edges) of every head against the row-restricted fp64 oracle, fp32 and bf16 gradients."""
+    B, H, N, d = 1, 3, 4093, 64
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=90 + causal, device=DEV, spike=True)
+    do = inputs.normal_bf16((B, H, N, d), seed=91, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    grads = {fp32: run_bwd(q, k, v, do, scale, causal, grad_fp32=fp32) for fp32 in (True, False)}
+    edge = [0, 63, 64, 127, 128, N - 62, N - 61, N - 1]
+    for h in range(H):
+        qr = np.unique(np.concatenate([inputs.sample_rows(N, 32, seed=200 + h).numpy(), edge]))
+        kr = np.unique(np.concatenate([inputs.sample_rows(N, 32, seed=300 + h).numpy(), edge]))
+        ref = oracle.attention_backward_rows(q[0, h].cpu(), k[0, h].cpu(), v[0, h].cpu(), do[0, h].cpu(), scale,
+                                             causal, q_rows=qr, k_rows=kr)
+        qi, ki = torch.from_numpy(qr).to(DEV), torch.from_numpy(kr).to(DEV)
+        for fp32, (dq, dk, dv) in grads.items():
+            got = (dq[0, h].index_select(0, qi), dk[0, h].index_select(0, ki), dv[0, h].index_select(0, ki))
+            assert_grads(got, ref, f"d=64 N={N} causal={causal} h={h} grad_fp32={fp32}")

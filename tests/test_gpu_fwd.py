@@ -152,3 +152,22 @@ def test_uneven_head_groups_cover_every_block(causal):
     o_ref, lse_ref = _oracle(q, k, v, scale, causal, rows=rows.numpy())
     o, lse = run_fwd(q, k, v, scale, causal, o_fp32=True)
     assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref, f"37 heads causal={causal}")
+
+
+@pytest.mark.parametrize("d,causal", [(64, True), (64, False), (128, False)])
+def test_long_spiky_sampled_rows(d, causal):
+    """Long sequences with x8 key spikes and a ragged last tile (N = 8189) on the schedules the
+    bench's workloads do not cover: d = 64 causal (separate P~, fwd_kernel<64, causal>), the
+    persistent d = 64 non-causal kernel over 64 key tiles per block, and d = 128 non-causal;
+    seeded rows plus tile edges of every head."""
+    B, H, N = 1, 6, 8189
+    q, k, v = inputs.prefill_inputs(B, H, N, d, seed=d + causal, device=DEV, spike=True)
+    scale = 1.0 / math.sqrt(d)
+    rows = inputs.sample_rows_per_head(B, H, N, 24, seed=8)
+    edge = torch.tensor([0, 127, 128, 255, 256, N - 126, N - 125, N - 1])
+    rows = torch.sort(torch.cat([rows, edge.expand(B, H, -1)], dim=2), dim=2).values
+    o_ref, lse_ref = _oracle(q, k, v, scale, causal, rows=rows.numpy())
+    for o_fp32 in (True, False):
+        o, lse = run_fwd(q, k, v, scale, causal, o_fp32=o_fp32)
+        assert_parity(gather_rows(o, rows), gather_rows(lse, rows), o_ref, lse_ref,
+                      f"d={d} N={N} causal={causal} o_fp32={o_fp32}")

@@ -14,14 +14,17 @@
 //
 // Warp roles (the producer/consumer split and the two-consumer "ping-pong" of
 // triton-tutorial §8.10.2-§8.10.3, re-done with TMA + tcgen05 + TMEM):
-//   warps 0-7  softmax of Q_0: two threads per query row, each with half of
-//              the row's 128 key columns (the .16x32bx2 TMEM access shape gives
-//              a warp 16 rows x both halves); the row max is joined with one
-//              shuffle, l is kept per half until the epilogue.  Whole rows stay
-//              inside one warp, so there is no cross-warp softmax merge
-//              (iceferryling "FlashAttention 1 和 FlashAttention 2 的区别", §7-8
-//              split-Q).  They also apply the alpha rescale of U_0 and write O_0, lse.
-//   warps 8-15 the same for Q_1.
+//   softmax of Q_0, then the same number of warps for Q_1: bf16 at d = 128 (P~
+//              aliasing S), 4 warps a tile, one thread per query row with all of
+//              its 128 key columns (.32x32b TMEM access, two 64-column loads, so
+//              that the max of the first half overlaps the second load); the
+//              separate-P~ schedules 8 warps a tile, two threads per row, each
+//              with half of the columns (.16x32bx2: a warp holds 16 rows x both
+//              halves), the row max joined with one shuffle and l kept per half
+//              until the epilogue.  Whole rows stay inside one warp, so there is
+//              no cross-warp softmax merge (iceferryling "FlashAttention 1 和
+//              FlashAttention 2 的区别", §7-8 split-Q).  They also apply the alpha
+//              rescale of U_t and write O_t, lse.
 //   MMA warp(s) one issuing thread each; the first also owns TMEM.
 //   last warp  TMA producer: Q_0, Q_1 once, then K_j and V_j into two rings.
 // Three schedules, by where P~ lives:
@@ -103,7 +106,12 @@ struct FwdCfg {
   // short for one issuing thread); with P~ aliasing S (bf16, d = 128) one MMA warp alternating
   // between the tiles measured faster.
   static constexpr bool TWO_ISSUERS = SEP;
-  static constexpr int WARP_TMA = kWarpMma + (TWO_ISSUERS ? 2 : 1);
+  // Softmax warps per query tile: with P~ aliasing S (bf16, d = 128) one thread per row (4 warps,
+  // .32x32b TMEM access); the separate-P~ schedules two threads per row (8 warps, .16x32bx2).
+  static constexpr bool ONE = !SEP;
+  static constexpr int SMW = ONE ? 4 : 8;
+  static constexpr int WARP_MMA = 2 * SMW;
+  static constexpr int WARP_TMA = WARP_MMA + (TWO_ISSUERS ? 2 : 1);
   static constexpr int THREADS = (WARP_TMA + 1) * 32;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2 * QB;
@@ -267,6 +275,130 @@ __device__ __forceinline__ void exp_pack_bf16(uint32_t (&sr)[64], uint64_t c2, u
   }
 }
 
+// One thread per row (d = 128): the row max over its 128 scores (sr: columns 0..63, sr2: 64..127,
+// raw fp32 bits; those from index `nvalid` on masked to -inf in place), in exponent units.
+__device__ __forceinline__ float row_max_full(uint32_t (&sr)[64], uint32_t (&sr2)[64], int nvalid, float m2, float c) {
+  if (nvalid < 128) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      if (i >= nvalid) sr[i] = __float_as_uint(-INFINITY);
+      if (64 + i >= nvalid) sr2[i] = __float_as_uint(-INFINITY);
+    }
+  }
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[k] = fmax3(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]), __uint_as_float(sr[8 + 2 * k]));
+    a[4 + k] = fmax3(__uint_as_float(sr2[2 * k]), __uint_as_float(sr2[2 * k + 1]), __uint_as_float(sr2[8 + 2 * k]));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[k] = fmaxf(a[k], __uint_as_float(sr[9 + 2 * k]));
+    a[4 + k] = fmaxf(a[4 + k], __uint_as_float(sr2[9 + 2 * k]));
+  }
+#pragma unroll
+  for (int i = 16; i < 64; i += 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      a[k] = fmax3(a[k], __uint_as_float(sr[i + 2 * k]), __uint_as_float(sr[i + 2 * k + 1]));
+      a[4 + k] = fmax3(a[4 + k], __uint_as_float(sr2[i + 2 * k]), __uint_as_float(sr2[i + 2 * k + 1]));
+    }
+  }
+  const float mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+  return fmaxf(m2, mx * c);
+}
+
+// One thread per row (d = 128): U_t row *= alpha in two TMEM round trips of 64 columns.
+__device__ __forceinline__ void rescale_row128(uint32_t taddr, float alpha) {
+  const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ur[64];
+    tmem_ld_x64(taddr + 64u * half, ur);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1])), a2), lo, hi);
+      ur[2 * i] = __float_as_uint(lo);
+      ur[2 * i + 1] = __float_as_uint(hi);
+    }
+    tmem_st_x64(taddr + 64u * half, ur);
+  }
+}
+
+// One thread per row (d = 128): O row = U / l as bf16 into the staged tile (box0: columns 0..63,
+// box1: 64..127, 128-byte swizzle), with the proxy fence the TMA store needs.
+__device__ __forceinline__ void stage_full_row_bf16(uint32_t box0, uint32_t box1, int r, uint32_t taddr, float mult) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ur[64];
+    tmem_ld_x64(taddr + 64u * half, ur);
+    const uint32_t srow = (half ? box1 : box0) + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t* u = ur + 8 * i;
+      sts128(srow + ((static_cast<uint32_t>(i) ^ static_cast<uint32_t>(r & 7)) << 4),
+             pack_bf16(__uint_as_float(u[0]) * mult, __uint_as_float(u[1]) * mult),
+             pack_bf16(__uint_as_float(u[2]) * mult, __uint_as_float(u[3]) * mult),
+             pack_bf16(__uint_as_float(u[4]) * mult, __uint_as_float(u[5]) * mult),
+             pack_bf16(__uint_as_float(u[6]) * mult, __uint_as_float(u[7]) * mult));
+    }
+  }
+  fence_proxy_async_smem();
+}
+
+// One thread per row (d = 128): O row = U / l (fp32 or bf16) and lse to global memory, rows < N.
+__device__ __forceinline__ void store_full_row(void* o, float* lse, size_t row_off, bool valid, bool o_fp32,
+                                               uint32_t taddr, float l, float m2) {
+  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ur[64];
+    tmem_ld_x64(taddr + 64u * half, ur);
+    if (!valid) continue;
+    if (o_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + row_off * 128 + 64 * half);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        dst[i] = make_float4(__uint_as_float(ur[4 * i]) * inv, __uint_as_float(ur[4 * i + 1]) * inv,
+                             __uint_as_float(ur[4 * i + 2]) * inv, __uint_as_float(ur[4 * i + 3]) * inv);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + row_off * 128 + 64 * half);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(ur[8 * i + 0]) * inv, __uint_as_float(ur[8 * i + 1]) * inv);
+        w.y = pack_bf16(__uint_as_float(ur[8 * i + 2]) * inv, __uint_as_float(ur[8 * i + 3]) * inv);
+        w.z = pack_bf16(__uint_as_float(ur[8 * i + 4]) * inv, __uint_as_float(ur[8 * i + 5]) * inv);
+        w.w = pack_bf16(__uint_as_float(ur[8 * i + 6]) * inv, __uint_as_float(ur[8 * i + 7]) * inv);
+        dst[i] = w;
+      }
+    }
+  }
+  if (valid) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
+}
+
+// One thread per row (d = 128): the key shard's partial (U, m, l) of the row, as store_half_partial.
+__device__ __forceinline__ void store_full_partial(const FwdAux& aux, size_t slot, bool valid, uint32_t taddr, float l,
+                                                   float m2) {
+  const bool empty = !(l > 0.f);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ur[64];
+    tmem_ld_x64(taddr + 64u * half, ur);
+    if (!valid || empty) continue;
+    float4* dst = reinterpret_cast<float4*>(aux.u_part + slot * 128 + 64 * half);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      dst[i] = make_float4(__uint_as_float(ur[4 * i]), __uint_as_float(ur[4 * i + 1]), __uint_as_float(ur[4 * i + 2]),
+                           __uint_as_float(ur[4 * i + 3]));
+  }
+  if (valid) {
+    aux.m_part[slot] = empty ? -INFINITY : m2 * kLn2;
+    aux.l_part[slot] = empty ? 0.f : l;
+  }
+}
+
 // lse of this thread's row from the h = 0 thread, rows < N only.
 __device__ __forceinline__ void store_lse(float* lse, size_t row_off, int h, bool valid, float l, float m2) {
   if (h == 0 && valid) lse[row_off] = (l > 0.f) ? (m2 + log2f(l)) * kLn2 : -INFINITY;
@@ -342,18 +474,18 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR(C::B_SF + t), 1);
-      mbar_init(BAR(C::B_PF + t), kSoftmaxWarps * 32);
-      mbar_init(BAR(C::B_SC + t), kSoftmaxWarps * 32);
+      mbar_init(BAR(C::B_PF + t), C::SMW * 32);
+      mbar_init(BAR(C::B_SC + t), C::SMW * 32);
       mbar_init(BAR(C::B_OF + t), 1);
     }
     mbar_init(BAR(C::B_DRAIN), 1);
     mbar_init(BAR(C::B_DRAIN + 1), 1);
-    mbar_init(BAR(C::B_OW), kSoftmaxWarps * 32);  // O of tile t staged (bf16 O)
-    mbar_init(BAR(C::B_OW + 1), kSoftmaxWarps * 32);
+    mbar_init(BAR(C::B_OW), C::SMW * 32);  // O of tile t staged (bf16 O)
+    mbar_init(BAR(C::B_OW + 1), C::SMW * 32);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == C::WARP_MMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -410,10 +542,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       for (int j = max(0, v_issued - C::VST); j < v_issued; ++j)
         drain_wait(BAR(C::B_VF + j % C::VST), (j / C::VST) & 1, budget);
     }
-  } else if (C::TWO_ISSUERS && (warp == kWarpMma || warp == kWarpMma + 1)) {
+  } else if (C::TWO_ISSUERS && (warp == C::WARP_MMA || warp == C::WARP_MMA + 1)) {
     // ------------------------------------------------------------ MMA issuer of one tile
     if (lane == 0) {
-      const int t = warp - kWarpMma;
+      const int t = warp - C::WARP_MMA;
       const int n = t ? n_t1 : n_t0;
       constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(kBr, kBc, 0) : idesc_bf16_f32(kBr, kBc, 0);
       constexpr uint32_t idesc_o = FP8 ? idesc_e4m3_f32(kBr, D, 1) : idesc_bf16_f32(kBr, D, 1);
@@ -503,7 +635,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         drain_wait(BAR(C::B_DRAIN + t), 0, budget);
       }
     }
-  } else if (!C::TWO_ISSUERS && warp == kWarpMma) {
+  } else if (!C::TWO_ISSUERS && warp == C::WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer for both tiles
     if constexpr (!C::TWO_ISSUERS) if (lane == 0) {
       // bf16, d = 128 (P~ aliasing S).  S = Q K^T (both K-major); U += P~ V (V MN-major).
@@ -585,15 +717,15 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       drain_wait(BAR(C::B_DRAIN), 0, budget);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 0-15
-    const int t = warp / kSoftmaxWarps;           // query tile of this warp
-    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
-    const int sub = (warp % kSoftmaxWarps) >> 2;  // which 16 lanes of the quarter
-    const int h = lane >> 4;                      // which half of the row's columns
-    const int r = 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = row within the tile
+    // ------------------------------------------------------------ softmax warps
+    const int t = warp / C::SMW;                 // query tile of this warp
+    const int quarter = warp & 3;                // TMEM lane quarter this warp may access
+    const int sub = C::ONE ? 0 : (warp % C::SMW) >> 2;  // which 16 lanes of the quarter (two threads a row)
+    const int h = C::ONE ? 0 : lane >> 4;        // which half of the row's columns (two threads a row)
+    const int r = C::ONE ? 32 * quarter + lane : 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = row
     const int row = pair * kRowsPerCta + t * kBr + r;
     const int n = t ? n_t1 : n_t0;
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(C::ONE ? 32 * quarter : 32 * quarter + 16 * sub) << 16;
     const uint32_t t_s = tmem + lane_addr + static_cast<uint32_t>(t * kBc);
     const uint32_t t_o = tmem + lane_addr + kColO + static_cast<uint32_t>(t * D);
     const uint32_t t_p = tmem + lane_addr + C::COL_P + 64u * t;  // separate P~ columns (d = 64)
@@ -620,14 +752,21 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       // exponent multiplier of this key tile: scale * log2(e), times the dequantization scales (FP8)
       const float cj = FP8 ? sq_t * sk_j * sl2 : sl2;
       const uint64_t c2 = f2_pack(cj, cj);
-      uint32_t sr[64];
-      tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
+      uint32_t sr[64], sr2[C::ONE ? 64 : 1];  // one thread a row: columns 0..63 in sr, 64..127 in sr2
+      if constexpr (C::ONE) {
+        tmem_ld_x64(t_s, sr);
+        tmem_ld_x64(t_s + 64, sr2);
+      } else {
+        tmem_ld2_x64<64>(t_s, sr);  // columns 64h .. 64h+63 of the row
+      }
       if constexpr (C::SEP) {
         tc_fence_before();
         mbar_arrive(BAR(C::B_SC + t));  // S_t(j) is in registers: the MMA may overwrite it
       }
-      // admissible keys among this thread's 64 columns
-      const float m_new = row_max_update(sr, lim - j * kBc - 64 * h + 1, m2, cj);
+      // admissible keys among this thread's 64 (128) columns
+      float m_new;
+      if constexpr (C::ONE) m_new = row_max_full(sr, sr2, lim - j * kBc + 1, m2, cj);
+      else m_new = row_max_update(sr, lim - j * kBc - 64 * h + 1, m2, cj);
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;  // fully-masked guard: alpha = p = 0
       const float alpha = ex2(m2 - mb);
       const uint64_t nmb2 = f2_pack(-mb, -mb);
@@ -681,19 +820,29 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         }
       }
       if constexpr (!C::SEP) {
-        // P~ packed in place into sr[0..31], then this thread's 32 packed columns (32h ..) of S_t
+        // P~ packed in place into sr[0..31] (and sr2[0..31]), then the row's 64 packed columns of
+        // S_t (keys 2i, 2i + 1 at column i), which its thread (or threads) have read
         exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);
-        uint32_t pr[32];
+        if constexpr (C::ONE) {
+          exp_pack_bf16(sr2, c2, nmb2, rs_a, rs_b);
+          tmem_st_x32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(sr));         // keys 0..63
+          tmem_st_x32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(sr2));   // keys 64..127
+        } else {
+          uint32_t pr[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pr[i] = sr[i];
-        tmem_st2_x32<32>(t_s, pr);
+          for (int i = 0; i < 32; ++i) pr[i] = sr[i];
+          tmem_st2_x32<32>(t_s, pr);
+        }
       }
       float s0, s1, s2, s3;
       f2_unpack(rs_a, s0, s1);
       f2_unpack(rs_b, s2, s3);
       l = fmaf(alpha, l, ((s0 + s1) + (s2 + s3)) * inv_ps);
       // PV_t(j-1) is complete (the commit that announced S_t(j) covers it): rescale U_t in place.
-      if (!C::SEP && j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
+      if (!C::SEP && j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
+        if constexpr (C::ONE) rescale_row128(t_o, alpha);
+        else rescale_half_row<D>(t_o, alpha);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(BAR(C::B_PF + t));
@@ -705,10 +854,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     }
     if (ok) {
       tc_fence_after();
-      const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      const float l_row = C::ONE ? l : l + __shfl_xor_sync(0xffffffffu, l, 16);
       if (aux.u_part) {
-        store_half_partial<D>(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, h, row < N, t_o, l_row,
-                              m2, true);
+        if constexpr (C::ONE)
+          store_full_partial(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, row < N, t_o, l_row, m2);
+        else
+          store_half_partial<D>(aux, (static_cast<size_t>(bh) * N + row) * aux.S + aux.shard, h, row < N, t_o, l_row,
+                                m2, true);
       } else if (!o_fp32) {
         // bf16 O through shared memory, in buffers this tile no longer reads: Q_t (its S MMAs are
         // complete), which has the O tile's shape for bf16 inputs; for E4M3 inputs Q_t and P~_t
@@ -717,9 +869,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         const uint32_t box0 = sQ + static_cast<uint32_t>(t) * C::QB;
         const uint32_t box1 = FP8 ? base + C::OFF_P + static_cast<uint32_t>(t) * C::PB : box0 + kBox;
         store_lse(lse, static_cast<size_t>(bh) * N + row, h, row < N, l_row, m2);
-        stage_half_row_bf16<D>(box0, box1, r, h, t_o, (l_row > 0.f) ? (FP8 ? sv_max * (1.f / 256.f) : 1.f) / l_row : 0.f);
+        const float o_mul = (l_row > 0.f) ? (FP8 ? sv_max * (1.f / 256.f) : 1.f) / l_row : 0.f;
+        if constexpr (C::ONE) stage_full_row_bf16(box0, box1, r, t_o, o_mul);
+        else stage_half_row_bf16<D>(box0, box1, r, h, t_o, o_mul);
         mbar_arrive(BAR(C::B_OW + t));
-        if ((warp % kSoftmaxWarps) == 0 && lane == 0 &&
+        if ((warp % C::SMW) == 0 && lane == 0 &&
             mbar_wait(BAR(C::B_OW + t), 0, abort_flag, budget, &g_fwd_status)) {
           for (int hb = 0; hb < D / 64; ++hb)
             tma_store_3d(&to, hb ? box1 : box0, hb * 64, pair * kRowsPerCta + t * kBr, bh);
@@ -727,8 +881,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           bulk_wait_all();  // complete before the CTA exits
         }
       } else {
-        store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
-                          FP8 ? sv_max * (1.f / 256.f) : 1.f);
+        if constexpr (C::ONE)
+          store_full_row(o, lse, static_cast<size_t>(bh) * N + row, row < N, o_fp32 != 0, t_o, l_row, m2);
+        else
+          store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
+                            FP8 ? sv_max * (1.f / 256.f) : 1.f);
       }
     } else if (aux.u_part && n == 0) {
       // no key of this shard is admissible for the tile: an empty partial, U never touched
@@ -740,7 +897,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 #undef BAR
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -14,9 +14,10 @@
 //
 // Both main kernels keep their own tile resident in shared memory, stream the
 // other side through a TMA ring, compute the two products of a step with
-// tcgen05.mma into TMEM, let 8 elementwise warps (two threads per row, the
-// .16x32bx2 TMEM shape) turn them into bf16 P^T and dS^T (or dS) in TMEM, and
-// accumulate the gradient MMAs (A operand from TMEM) into TMEM.  The gradient
+// tcgen05.mma into TMEM, let the elementwise warps (one thread per row at
+// d = 128, two at d = 64) turn them into bf16 P^T and dS^T (or dS) in TMEM,
+// chunk by chunk, and accumulate the gradient MMAs (A operand from TMEM) into
+// TMEM, each chunk's as soon as it is ready.  The gradient
 // MMAs of step i and the products of step i+1 are issued back to back; the
 // tensor core runs them in order, so the products may overwrite the TMEM
 // columns the gradient MMAs read.
@@ -35,10 +36,17 @@ namespace {
 
 constexpr int kTile = 128;                // rows per tile on either side
 constexpr uint32_t kBox = 128u * 128u;    // bytes of a 128-row x 64-column bf16 box
-constexpr int kEwWarps = 8;               // elementwise warps: two threads per row
-constexpr int kWarpMma = kEwWarps, kWarpTma = kEwWarps + 1;
-constexpr int kThreads = (kEwWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 512;
+// Elementwise warps of the dK/dV and dQ kernels: at d = 128 one thread per (key or query) row (4
+// warps, .32x32b TMEM access, the row's 128 columns in four chunks of 32); at d = 64 8 warps, two
+// threads a row (.16x32bx2, two chunks; the dK/dV kernel takes each query tile in two halves).
+template <int D>
+struct BwdWarps {
+  static constexpr bool ONE = D == 128;
+  static constexpr int EW = ONE ? 4 : 8;
+  static constexpr int CHUNKS = ONE ? 4 : 2;
+  static constexpr int MMA = EW, TMA = EW + 1, THREADS = (EW + 2) * 32;
+};
 constexpr uint32_t kColA = 0, kColB = 128, kColG1 = 256;  // products at 0 / 128, gradients from 256
 constexpr uint32_t kColS1 = 384;  // dQ kernel: second S buffer (S(j) at kColA for even j, here for odd j)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -60,6 +68,12 @@ __device__ __forceinline__ void bdrain(uint32_t bar, uint32_t parity, unsigned l
       return;
     }
   }
+}
+
+__device__ __forceinline__ void tmem_st1_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                  "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
 }
 
 // --------------------------------------------------------------------- D = rowsum(O * dO)
@@ -126,6 +140,40 @@ __device__ __forceinline__ void store_grad_half_row(void* out, size_t row_off, i
   }
 }
 
+// d = 128, one thread per row: a 128-column fp32 tile row in TMEM * scale -> global (fp32), or as
+// bf16 into the staged tile (box0: columns 0..63, box1: 64..127, 128-byte swizzle).
+__device__ __forceinline__ void store_grad_row128(void* out, size_t row_off, bool valid, uint32_t taddr, float scale) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ur[64];
+    tmem_ld_x64(taddr + 64u * half, ur);
+    if (!valid) continue;
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off * 128 + 64 * half);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      dst[i] = make_float4(__uint_as_float(ur[4 * i]) * scale, __uint_as_float(ur[4 * i + 1]) * scale,
+                           __uint_as_float(ur[4 * i + 2]) * scale, __uint_as_float(ur[4 * i + 3]) * scale);
+  }
+}
+__device__ __forceinline__ void stage_row128_bf16(uint32_t box0, uint32_t box1, int r, uint32_t taddr, float scale) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ur[64];
+    tmem_ld_x64(taddr + 64u * half, ur);
+    const uint32_t srow = (half ? box1 : box0) + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t* u = ur + 8 * i;
+      sts128(srow + ((static_cast<uint32_t>(i) ^ static_cast<uint32_t>(r & 7)) << 4),
+             pack_bf16(__uint_as_float(u[0]) * scale, __uint_as_float(u[1]) * scale),
+             pack_bf16(__uint_as_float(u[2]) * scale, __uint_as_float(u[3]) * scale),
+             pack_bf16(__uint_as_float(u[4]) * scale, __uint_as_float(u[5]) * scale),
+             pack_bf16(__uint_as_float(u[6]) * scale, __uint_as_float(u[7]) * scale));
+    }
+  }
+  fence_proxy_async_smem();
+}
+
 // S = A B^T into TMEM: A and B are resident/streamed 128 x d K-major tiles.
 template <int D>
 __device__ __forceinline__ void issue_product(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t idesc) {
@@ -154,6 +202,20 @@ __device__ __forceinline__ void issue_grad_part(uint32_t d_tmem, uint32_t a_tmem
   for (int q = 0; q < 4; ++q) {
     const int kk = 2 * part + (q & 1) + 4 * (q >> 1);
     const uint32_t a = a_tmem + packed_col(kk);
+    const uint64_t b = sdesc_add(db, static_cast<uint32_t>(kk) * 2048u);
+    if (q == 0 && !accumulate) mma_ts_c<0>(d_tmem, a, b, idesc);
+    else mma_ts_c<1>(d_tmem, a, b, idesc);
+  }
+}
+
+// G (+)= X Y for chunk c of the one-thread-per-row dK/dV kernel (d = 128): K blocks 2c, 2c + 1,
+// packed at columns 8kk (each thread packs its chunk c into columns 16c .., which it has read).
+__device__ __forceinline__ void issue_grad_chunk(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idesc,
+                                                 bool accumulate, int c) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int kk = 2 * c + q;
+    const uint32_t a = a_tmem + 8u * static_cast<uint32_t>(kk);
     const uint64_t b = sdesc_add(db, static_cast<uint32_t>(kk) * 2048u);
     if (q == 0 && !accumulate) mma_ts_c<0>(d_tmem, a, b, idesc);
     else mma_ts_c<1>(d_tmem, a, b, idesc);
@@ -242,14 +304,14 @@ struct DkdvCfg : BwdCfg<D> {
   // B_SF (+ q): products (of query half q) ready; B_PF + c: elementwise chunk (half) c done;
   // B_GF: gradients final
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 2,
-                       B_GF = B_PF + 2, B_DRAIN = B_GF + 1, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;
+                       B_GF = B_PF + 4, B_DRAIN = B_GF + 1, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
 };
 static_assert(DkdvCfg<128>::SMEM <= 232448, "dK/dV kernel shared memory");
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwdWarps<D>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dk,
@@ -257,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     unsigned long long budget, const __grid_constant__ CUtensorMap tdk,
                     const __grid_constant__ CUtensorMap tdv, int ng) {
   using C = DkdvCfg<D>;
+  using W = BwdWarps<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -282,15 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::B_SF), 1);
     mbar_init(BAR(C::B_SF + 1), 1);
-    mbar_init(BAR(C::B_PF), kEwWarps * 32);
-    mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
+    for (int c = 0; c < W::CHUNKS; ++c) mbar_init(BAR(C::B_PF + c), W::EW * 32);
     mbar_init(BAR(C::B_GF), 1);
     mbar_init(BAR(C::B_DRAIN), 1);
-    mbar_init(BAR(C::B_OW), kEwWarps * 32);  // bf16 gradients staged
+    mbar_init(BAR(C::B_OW), W::EW * 32);  // bf16 gradients staged
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == W::MMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -299,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == kWarpTma) {
+  if (warp == W::TMA) {
     // ------------------------------------------------------------ producer (whole warp)
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -343,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bdrain(BAR(C::B_KV), 0, budget);
       for (int i = max(0, issued - C::ST); i < issued; ++i) bdrain(BAR(C::B_FULL + i % C::ST), (i / C::ST) & 1, budget);
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == W::MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       if constexpr (C::HALVES) {
@@ -416,16 +478,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; ok && i < n_i; ++i) {
           const uint32_t st = (i % C::ST) * C::STAGE;
           bool part_ok = true;
-          for (int part = 0; part < 2; ++part) {  // each half as soon as the elementwise warps finish it
+          for (int part = 0; part < W::CHUNKS; ++part) {  // each chunk as soon as the elementwise warps finish it
             if (!bwait(BAR(C::B_PF + part), i & 1, abort_flag, budget)) {
               part_ok = false;
               break;
             }
             tc_fence_after();
-            issue_grad_part<D>(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0 || part > 0,
-                               part);  // dV += P^T dO
-            issue_grad_part<D>(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0 || part > 0,
-                               part);  // dK += dS^T Q
+            issue_grad_chunk(tmem + kColG1, tmem + kColA, sdesc_add(dRmn, st + C::TB), idesc_g, i > 0 || part > 0,
+                             part);  // dV += P^T dO
+            issue_grad_chunk(tmem + C::COL_G2, tmem + kColB, sdesc_add(dRmn, st), idesc_g, i > 0 || part > 0,
+                             part);  // dK += dS^T Q
           }
           if (!part_ok) break;
           tc_commit(BAR(C::B_EMPTY + i % C::ST));
@@ -443,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise warps: thread = key row
-    const int quarter = warp & 3, sub = warp >> 2, h = lane >> 4;
-    const int r = 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = key row within the tile
+    const int quarter = warp & 3, sub = W::ONE ? 0 : warp >> 2, h = W::ONE ? 0 : lane >> 4;
+    const int r = W::ONE ? 32 * quarter + lane : 32 * quarter + 16 * sub + (lane & 15);  // TMEM lane = key row
     const int key = kt * kTile + r;
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(W::ONE ? 32 * quarter : 32 * quarter + 16 * sub) << 16;
     const uint32_t tA = tmem + lane_addr + kColA, tB = tmem + lane_addr + kColB;
     const uint64_t c2 = f2_pack(sl2, sl2);
     bool ok = true;
@@ -487,17 +549,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* nv = reinterpret_cast<const float4*>(vec + s * (2 * kTile));
         // Causal: only the diagonal query tile (qt == kt) holds pairs with query < key.
         const bool diag = CAUSAL && qt == kt;
-        // this thread's 64 query columns, two chunks of 32
+        // this thread's row: its 128 query columns in four chunks of 32, chunk c packed into
+        // columns 16c .. 16c + 15 (all read by this thread already)
   #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t sv[32], pv[32];
-          tmem_ld2_x32<64>(tA + 32 * c, sv);
-          tmem_ld2_x32<64>(tB + 32 * c, pv);
+          tmem_ld_x32(tA + 32 * c, sv);
+          tmem_ld_x32(tB + 32 * c, pv);
           uint32_t pp[16], dp[16];
-          if (diag) ew_pairs_dkdv<true>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
-          else ew_pairs_dkdv<false>(sv, pv, nv, c2, 64 * h + 32 * c, qt * kTile, key, pp, dp);
-          tmem_st2_x16<64>(tA + 16 * c, pp);  // P^T packed: columns 64h + 16c ..
-          tmem_st2_x16<64>(tB + 16 * c, dp);  // dS^T packed
+          if (diag) ew_pairs_dkdv<true>(sv, pv, nv, c2, 32 * c, qt * kTile, key, pp, dp);
+          else ew_pairs_dkdv<false>(sv, pv, nv, c2, 32 * c, qt * kTile, key, pp, dp);
+          tmem_st1_x16(tA + 16 * c, pp);  // P^T packed
+          tmem_st1_x16(tB + 16 * c, dp);  // dS^T packed
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
@@ -509,13 +572,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const size_t row_off = static_cast<size_t>(bh) * N + key;
       if (grad_fp32) {
-        store_grad_half_row<D>(dv, row_off, h, key < N, true, tmem + lane_addr + kColG1, 1.f);
-        store_grad_half_row<D>(dk, row_off, h, key < N, true, tmem + lane_addr + C::COL_G2, scale);
+        if constexpr (W::ONE) {
+          store_grad_row128(dv, row_off, key < N, tmem + lane_addr + kColG1, 1.f);
+          store_grad_row128(dk, row_off, key < N, tmem + lane_addr + C::COL_G2, scale);
+        } else {
+          store_grad_half_row<D>(dv, row_off, h, key < N, true, tmem + lane_addr + kColG1, 1.f);
+          store_grad_half_row<D>(dk, row_off, h, key < N, true, tmem + lane_addr + C::COL_G2, scale);
+        }
       } else {
         // bf16 dV and dK through shared memory: the V and K tiles have their shape and are no
         // longer read (every product MMA is complete); one thread stores them with TMA.
-        stage_half_row_bf16<D>(sV, sV + kBox, r, h, tmem + lane_addr + kColG1, 1.f);
-        stage_half_row_bf16<D>(sK, sK + kBox, r, h, tmem + lane_addr + C::COL_G2, scale);
+        if constexpr (W::ONE) {
+          stage_row128_bf16(sV, sV + kBox, r, tmem + lane_addr + kColG1, 1.f);
+          stage_row128_bf16(sK, sK + kBox, r, tmem + lane_addr + C::COL_G2, scale);
+        } else {
+          stage_half_row_bf16<D>(sV, sV + kBox, r, h, tmem + lane_addr + kColG1, 1.f);
+          stage_half_row_bf16<D>(sK, sK + kBox, r, h, tmem + lane_addr + C::COL_G2, scale);
+        }
         mbar_arrive(BAR(C::B_OW));
         if (warp == 0 && lane == 0 && bwait(BAR(C::B_OW), 0, abort_flag, budget)) {
           for (int hb = 0; hb < C::NH; ++hb) {
@@ -532,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef BAR
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == W::MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -548,7 +621,7 @@ struct DqCfg : BwdCfg<D> {
   static constexpr uint32_t STAGE = 2 * B::TB;
   static constexpr uint32_t OFF_BAR = OFF_RING + B::ST * STAGE;
   static constexpr int B_QD = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 1,
-                       B_DRAIN = B_PF + 2, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;  // B_PF + c: chunk c of the
+                       B_DRAIN = B_PF + 4, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;  // B_PF + c: chunk c of the
                                                                                // elementwise step
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;
@@ -556,13 +629,14 @@ struct DqCfg : BwdCfg<D> {
 static_assert(DqCfg<128>::SMEM <= 232448, "dQ kernel shared memory");
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwdWarps<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const float* __restrict__ lse, const float* __restrict__ delta, void* __restrict__ dq, int N,
                   float sl2, float scale, int grad_fp32, unsigned long long budget,
                   const __grid_constant__ CUtensorMap tdq, int ng) {
   using C = DqCfg<D>;
+  using W = BwdWarps<D>;  // thread = query row here
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -586,14 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::B_EMPTY + s), 1);
     }
     mbar_init(BAR(C::B_SF), 1);
-    mbar_init(BAR(C::B_PF), kEwWarps * 32);
-    mbar_init(BAR(C::B_PF + 1), kEwWarps * 32);
+    for (int c = 0; c < W::CHUNKS; ++c) mbar_init(BAR(C::B_PF + c), W::EW * 32);
     mbar_init(BAR(C::B_DRAIN), 1);
-    mbar_init(BAR(C::B_OW), kEwWarps * 32);  // bf16 gradients staged
+    mbar_init(BAR(C::B_OW), W::EW * 32);  // bf16 gradients staged
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == W::MMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -602,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == kWarpTma) {
+  if (warp == W::TMA) {
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -628,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bdrain(BAR(C::B_QD), 0, budget);
       for (int j = max(0, issued - C::ST); j < issued; ++j) bdrain(BAR(C::B_FULL + j % C::ST), (j / C::ST) & 1, budget);
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == W::MMA) {
     if (lane == 0) {
       constexpr uint32_t idesc_p = idesc_bf16_f32(kTile, kTile, 0);  // Q K^T, dO V^T: both K-major
       constexpr uint32_t idesc_g = idesc_bf16_f32(kTile, D, 1);      // dS K: K MN-major
@@ -657,16 +730,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // then the second chunk's dQ MMAs and dP(j+1).
         if (!bwait(BAR(C::B_PF), j & 1, abort_flag, budget)) break;
         tc_fence_after();
-        issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, j > 0,
-                           0);
+        if constexpr (W::ONE)
+          issue_grad_chunk(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, j > 0, 0);
+        else
+          issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, j > 0,
+                             0);
         if (j + 1 < n_j) {
           if (!bwait(BAR(C::B_FULL + (j + 1) % C::ST), ((j + 1) / C::ST) & 1, abort_flag, budget)) break;
           tc_fence_after();
           issue_s(j + 1);
         }
-        if (!bwait(BAR(C::B_PF + 1), j & 1, abort_flag, budget)) break;
-        tc_fence_after();
-        issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, true, 1);
+        bool chunks_ok = true;
+        for (int c = 1; c < W::CHUNKS; ++c) {
+          if (!bwait(BAR(C::B_PF + c), j & 1, abort_flag, budget)) {
+            chunks_ok = false;
+            break;
+          }
+          tc_fence_after();
+          if constexpr (W::ONE)
+            issue_grad_chunk(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, true, c);
+          else
+            issue_grad_part<D>(tmem + kColG1, tmem + kColB, sdesc_add(dRmn, (j % C::ST) * C::STAGE), idesc_g, true,
+                               c);
+        }
+        if (!chunks_ok) break;
         tc_commit(BAR(C::B_EMPTY + j % C::ST));
         if (j + 1 < n_j) issue_dp(j + 1);
         tc_commit(BAR(C::B_SF));
@@ -676,10 +763,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise warps: thread = query row
-    const int quarter = warp & 3, sub = warp >> 2, h = lane >> 4;
-    const int r = 32 * quarter + 16 * sub + (lane & 15);
+    const int quarter = warp & 3, sub = W::ONE ? 0 : warp >> 2, h = W::ONE ? 0 : lane >> 4;
+    const int r = W::ONE ? 32 * quarter + lane : 32 * quarter + 16 * sub + (lane & 15);
     const int row = qt * kTile + r;
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(W::ONE ? 32 * quarter : 32 * quarter + 16 * sub) << 16;
     const uint32_t tB = tmem + lane_addr + kColB;  // dP; S(j) is in buffer j % 2 (kColA, kColS1)
     const bool in = row < N;
     const float lse2 = in ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : INFINITY;
@@ -691,30 +778,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = bwait_all(BAR(C::B_SF), j & 1, abort_flag, budget);
       if (!ok) break;
       tc_fence_after();
+      if constexpr (W::ONE) {
+        // this thread's row: 128 keys in four chunks of 32, chunk c's dS packed into dP's columns
+        // 16c .. 16c + 15 (read by this thread already)
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], pv[32];
-        tmem_ld2_x32<64>(tmem + lane_addr + ((j & 1) ? kColS1 : kColA) + 32 * c, sv);
-        tmem_ld2_x32<64>(tB + 32 * c, pv);
-        uint32_t dp[16];
-        const int key0 = j * kTile + 64 * h + 32 * c;
-        // only the diagonal and the ragged last key tile reach past this row's last key
-        if (key0 + 31 > lim) ew_pairs_dq<true>(sv, pv, c2, nl2, nd2, key0, lim, dp);
-        else ew_pairs_dq<false>(sv, pv, c2, nl2, nd2, key0, lim, dp);
-        tmem_st2_x16<64>(tB + 16 * c, dp);  // dS packed into dP's columns 64h + 16c ..
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], pv[32];
+          tmem_ld_x32(tmem + lane_addr + ((j & 1) ? kColS1 : kColA) + 32 * c, sv);
+          tmem_ld_x32(tB + 32 * c, pv);
+          uint32_t dp[16];
+          const int key0 = j * kTile + 32 * c;
+          if (key0 + 31 > lim) ew_pairs_dq<true>(sv, pv, c2, nl2, nd2, key0, lim, dp);
+          else ew_pairs_dq<false>(sv, pv, c2, nl2, nd2, key0, lim, dp);
+          tmem_st1_x16(tB + 16 * c, dp);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32], pv[32];
+          tmem_ld2_x32<64>(tmem + lane_addr + ((j & 1) ? kColS1 : kColA) + 32 * c, sv);
+          tmem_ld2_x32<64>(tB + 32 * c, pv);
+          uint32_t dp[16];
+          const int key0 = j * kTile + 64 * h + 32 * c;
+          // only the diagonal and the ragged last key tile reach past this row's last key
+          if (key0 + 31 > lim) ew_pairs_dq<true>(sv, pv, c2, nl2, nd2, key0, lim, dp);
+          else ew_pairs_dq<false>(sv, pv, c2, nl2, nd2, key0, lim, dp);
+          tmem_st2_x16<64>(tB + 16 * c, dp);  // dS packed into dP's columns 64h + 16c ..
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(BAR(C::B_PF + c));  // chunk c ready: its gradient MMAs may start
+        }
       }
     }
     if (ok) ok = bwait_all(BAR(C::B_SF), n_j & 1, abort_flag, budget);
     if (ok) {
       tc_fence_after();
       if (grad_fp32) {
-        store_grad_half_row<D>(dq, static_cast<size_t>(bh) * N + row, h, in, true, tmem + lane_addr + kColG1, scale);
+        if constexpr (W::ONE) store_grad_row128(dq, static_cast<size_t>(bh) * N + row, in, tmem + lane_addr + kColG1, scale);
+        else store_grad_half_row<D>(dq, static_cast<size_t>(bh) * N + row, h, in, true, tmem + lane_addr + kColG1, scale);
       } else {
         // bf16 dQ through shared memory: the Q tile has its shape and is no longer read
-        stage_half_row_bf16<D>(sQ, sQ + kBox, r, h, tmem + lane_addr + kColG1, scale);
+        if constexpr (W::ONE) stage_row128_bf16(sQ, sQ + kBox, r, tmem + lane_addr + kColG1, scale);
+        else stage_half_row_bf16<D>(sQ, sQ + kBox, r, h, tmem + lane_addr + kColG1, scale);
         mbar_arrive(BAR(C::B_OW));
         if (warp == 0 && lane == 0 && bwait(BAR(C::B_OW), 0, abort_flag, budget)) {
           for (int hb = 0; hb < C::NH; ++hb)
@@ -729,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef BAR
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == W::MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -749,13 +857,13 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
   auto k1 = bwd_dkdv_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM)) != cudaSuccess)
     return e;
-  k1<<<grid, kThreads, DkdvCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dk, a.dv, a.N,
+  k1<<<grid, BwdWarps<D>::THREADS, DkdvCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dk, a.dv, a.N,
                                                    a.scale_log2, a.scale, a.grad_fp32, a.budget, a.tdk, a.tdv, ng);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto k2 = bwd_dq_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM)) != cudaSuccess)
     return e;
-  k2<<<grid, kThreads, DqCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dq, a.N, a.scale_log2,
+  k2<<<grid, BwdWarps<D>::THREADS, DqCfg<D>::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.lse, a.delta, a.dq, a.N, a.scale_log2,
                                                  a.scale, a.grad_fp32, a.budget, a.tdq, ng);
   return cudaGetLastError();
 }

@@ -37,9 +37,8 @@
 //     (384 + 64t) and one MMA warp per tile issues S_t(j+1) as soon as the softmax
 //     has read S_t(j) ("separate P~"); the softmax waits for PV_t(j-1) only before
 //     overwriting P~_t and rescaling U_t.
-//   E4M3, d = 128: TMEM is laid out as for bf16 d = 128, but shared memory has room
-//     for P~ (16 KB a tile): the separate-P~ schedule with P~ in shared memory, read
-//     by the PV MMA as an SS operand.
+//   E4M3, d = 128: as bf16 d = 128, with P~ packed four keys a column into its S
+//     (32 columns a row) and the PV MMA kind::f8f6f4 reading it from TMEM.
 //
 // Two kernels share these schedules.  fwd_kernel runs one CTA per block of 256 query rows
 // (causal launches order the blocks longest first).  fwd_persist_kernel (non-causal bf16,
@@ -95,13 +94,13 @@ struct FwdCfg {
                        B_SF = B_VE + VST, B_PF = B_SF + 2, B_SC = B_PF + 2, B_OF = B_SC + 2, B_DRAIN = B_OF + 2,
                        B_OSF = B_DRAIN + 2, B_OW = B_OSF + 2, NBAR = B_OW + 2;
   // d = 64 leaves 128 TMEM columns free: P~_t gets its own columns there, so S_t(j+1) can be
-  // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S.
-  // E4M3 (d = 128): TMEM has no room for separate P~ columns, but shared memory has (16 KB a
-  // tile), so P~ goes there and PV reads it as an SS MMA.
-  static constexpr bool SEP = (D == 64) || FP8;
+  // computed while the softmax of tile j still runs ("separate P~").  At d = 128 P~ aliases S,
+  // for bf16 (two keys a column) and E4M3 (four keys a column) alike.
+  static constexpr bool SEP = D == 64;
+  // E4M3: a second 16 KB box per tile, which with the Q tile's stages O in bf16 (128 x 256 bytes)
   static constexpr bool P_SMEM = FP8;
-  static constexpr uint32_t COL_P = (SEP && !P_SMEM) ? 384u : 0u;  // + 64 t (TMEM, separate) or + 128 t (aliased)
-  static constexpr uint32_t PB = P_SMEM ? kBr * 128u : 0u;           // bytes of one tile's P~ in shared memory
+  static constexpr uint32_t COL_P = SEP ? 384u : 0u;        // separate P~ columns (+ 64 t)
+  static constexpr uint32_t PB = P_SMEM ? kBr * 128u : 0u;  // bytes of one tile's second O staging box (E4M3)
   // With separate P~ each tile gets its own MMA warp (at d = 64 the PV MMAs, N = 64, are also too
   // short for one issuing thread); with P~ aliasing S (bf16, d = 128) one MMA warp alternating
   // between the tiles measured faster.
@@ -116,7 +115,7 @@ struct FwdCfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2 * QB;
   static constexpr uint32_t OFF_V = OFF_K + KST * KVB;
-  static constexpr uint32_t OFF_P = OFF_V + VST * KVB;       // P~ of both tiles (E4M3 only)
+  static constexpr uint32_t OFF_P = OFF_V + VST * KVB;       // E4M3 only: O staging boxes of both tiles
   static constexpr uint32_t OFF_BAR = OFF_P + 2 * PB;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;  // TMEM address slot, abort flag
   static constexpr uint32_t SMEM = OFF_MISC + 16u + 1024u;   // + slack to align the base to 1 KB
@@ -349,8 +348,8 @@ __device__ __forceinline__ void stage_full_row_bf16(uint32_t box0, uint32_t box1
 
 // One thread per row (d = 128): O row = U / l (fp32 or bf16) and lse to global memory, rows < N.
 __device__ __forceinline__ void store_full_row(void* o, float* lse, size_t row_off, bool valid, bool o_fp32,
-                                               uint32_t taddr, float l, float m2) {
-  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+                                               uint32_t taddr, float l, float m2, float o_mult) {
+  const float inv = (l > 0.f) ? o_mult / l : 0.f;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t ur[64];
@@ -545,14 +544,15 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   } else if (C::TWO_ISSUERS && (warp == C::WARP_MMA || warp == C::WARP_MMA + 1)) {
     // ------------------------------------------------------------ MMA issuer of one tile
     if (lane == 0) {
+      // bf16 (the separate-P~ schedule is d = 64 only)
+      static_assert(!(FP8 && C::TWO_ISSUERS), "E4M3 runs the schedule with P~ aliasing S");
       const int t = warp - C::WARP_MMA;
       const int n = t ? n_t1 : n_t0;
-      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(kBr, kBc, 0) : idesc_bf16_f32(kBr, kBc, 0);
-      constexpr uint32_t idesc_o = FP8 ? idesc_e4m3_f32(kBr, D, 1) : idesc_bf16_f32(kBr, D, 1);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
       const uint64_t dq = sdesc_add(sdesc_sw128(sQ, 16, 1024), t * C::QB);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
-      const uint64_t dp = sdesc_sw128(base + C::OFF_P + t * C::PB, 16, 1024);  // E4M3 P~: K-major, one box
       const uint32_t d_s = tmem + t * kBc;
       const uint32_t d_o = tmem + kColO + t * D;
       const uint32_t a_p = tmem + (C::SEP ? C::COL_P + 64u * t : static_cast<uint32_t>(t * kBc));
@@ -561,28 +561,19 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < C::ROW / 32; ++kk) {  // 32 bytes of K per MMA
           const uint32_t off = static_cast<uint32_t>(kk >> 2) * kBox + static_cast<uint32_t>(kk & 3) * 32u;
-          if constexpr (FP8) {
-            if (kk == 0) mma_ss_f8_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
-            else mma_ss_f8_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
-          } else {
-            if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
-            else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
-          }
+          if (kk == 0) mma_ss_c<0>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
+          else mma_ss_c<1>(d_s, sdesc_add(dq, off), sdesc_add(dk, off), idesc_s);
         }
       };
       auto issue_pv = [&](int j) {
         const uint64_t dv = sdesc_add(dv0, (j % C::VST) * C::KVB);
 #pragma unroll
         for (int kk = 0; kk < kBc / C::K_MMA; ++kk) {
-          // K_MMA keys per MMA: K_MMA rows x 128 B of each V box
+          // K_MMA keys per MMA: K_MMA rows x 128 B of each V box; A = P~ in TMEM, 8 columns (16
+          // bf16 keys) per MMA
           const uint64_t b = sdesc_add(dv, static_cast<uint32_t>(kk * C::K_MMA) * 128u);
-          if constexpr (C::P_SMEM) {  // A = P~ rows in shared memory, 32 bytes (keys) per MMA
-            if (j > 0 || kk > 0) mma_ss_f8_c<1>(d_o, sdesc_add(dp, 32u * kk), b, idesc_o);
-            else mma_ss_f8_c<0>(d_o, sdesc_add(dp, 32u * kk), b, idesc_o);
-          } else {                    // A = P~ in TMEM, 8 columns (16 bf16 keys) per MMA
-            if (j > 0 || kk > 0) mma_ts_c<1>(d_o, a_p + 8u * kk, b, idesc_o);
-            else mma_ts_c<0>(d_o, a_p + 8u * kk, b, idesc_o);
-          }
+          if (j > 0 || kk > 0) mma_ts_c<1>(d_o, a_p + 8u * kk, b, idesc_o);
+          else mma_ts_c<0>(d_o, a_p + 8u * kk, b, idesc_o);
         }
       };
       auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -638,19 +629,27 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
   } else if (!C::TWO_ISSUERS && warp == C::WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer for both tiles
     if constexpr (!C::TWO_ISSUERS) if (lane == 0) {
-      // bf16, d = 128 (P~ aliasing S).  S = Q K^T (both K-major); U += P~ V (V MN-major).
-      static_assert(!FP8 && !C::SEP, "one MMA warp for both tiles only with P~ aliasing S (bf16)");
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBr, kBc, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBr, D, 1);
+      // d = 128 (P~ aliasing S), bf16 or E4M3.  S = Q K^T (both K-major); U += P~ V (V MN-major).
+      static_assert(!C::SEP, "one MMA warp for both tiles only with P~ aliasing S");
+      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(kBr, kBc, 0) : idesc_bf16_f32(kBr, kBc, 0);
+      constexpr uint32_t idesc_o = FP8 ? idesc_e4m3_f32(kBr, D, 1) : idesc_bf16_f32(kBr, D, 1);
       // Descriptors computed once; each MMA below is one 32-bit add plus the tcgen05.mma.
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, kBox, 1024);
       auto mma_s = [&](bool acc, uint32_t d, uint64_t a, uint64_t b) {
-        if (acc) mma_ss_c<1>(d, a, b, idesc_s); else mma_ss_c<0>(d, a, b, idesc_s);
+        if constexpr (FP8) {
+          if (acc) mma_ss_f8_c<1>(d, a, b, idesc_s); else mma_ss_f8_c<0>(d, a, b, idesc_s);
+        } else {
+          if (acc) mma_ss_c<1>(d, a, b, idesc_s); else mma_ss_c<0>(d, a, b, idesc_s);
+        }
       };
       auto mma_o = [&](bool acc, uint32_t d, uint32_t a, uint64_t b) {
-        if (acc) mma_ts_c<1>(d, a, b, idesc_o); else mma_ts_c<0>(d, a, b, idesc_o);
+        if constexpr (FP8) {
+          if (acc) mma_ts_f8_c<1>(d, a, b, idesc_o); else mma_ts_f8_c<0>(d, a, b, idesc_o);
+        } else {
+          if (acc) mma_ts_c<1>(d, a, b, idesc_o); else mma_ts_c<0>(d, a, b, idesc_o);
+        }
       };
       auto issue_s = [&](int t, int j) {
         const uint64_t dq = sdesc_add(dq0, t * C::QB);
@@ -773,29 +772,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
       uint64_t rs_a = f2_pack(0.f, 0.f), rs_b = rs_a;
       float inv_ps = 1.f;  // FP8: the row sum below is of p * ps; l takes p
       if constexpr (C::SEP) {
-        if constexpr (FP8) {
-          // P~ as E4M3 of p * ps, ps = 256 * sv_j / sv_max (<= 256): the V block scale rides on P~
-          // so that U accumulates in one unit for every key tile.  ps is folded into the exponent:
-          // p * ps = 2^(s c - m + log2 ps).  Packed in place into sr[0..15] (entry i: keys 64h + 4i ..).
-          const float ps = 256.f * sv_j / sv_max;
-          inv_ps = sv_max / (256.f * sv_j);
-          const float lps = log2f(ps);
-          const uint64_t nmp2 = f2_pack(lps - mb, lps - mb);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1, x2, x3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2, nmp2), x0,
-                      x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2, nmp2), x2,
-                      x3);
-            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-            rs_a = f2_add(rs_a, f2_pack(p0, p1));
-            rs_b = f2_add(rs_b, f2_pack(p2, p3));
-            sr[i] = pack_e4m3x4(p0, p1, p2, p3);
-          }
-        } else {
-          exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);  // P~ packed in place into sr[0..31]
-        }
+        exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);  // P~ packed in place into sr[0..31]
         // PV_t(j-1) must be done before P~_t(j) overwrites P~_t(j-1) and before U_t is rescaled.
         if (j > 0) {
           ok = wait_all(BAR(C::B_OF + t), (j - 1) & 1, abort_flag, budget);
@@ -803,23 +780,35 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
           tc_fence_after();
           if (!__all_sync(0xffffffffu, alpha == 1.f)) rescale_half_row<D>(t_o, alpha);
         }
-        if constexpr (C::P_SMEM) {
-          // row r of this tile's P~ (128 E4M3 keys = 128 bytes, 128-byte swizzle); this thread's
-          // keys 64h .. 64h + 63 are 16-byte chunks 4h .. 4h + 3
-          const uint32_t prow = base + C::OFF_P + t * C::PB + static_cast<uint32_t>(r) * 128u;
+        uint32_t pr[32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sts128(prow + ((static_cast<uint32_t>(4 * h + i) ^ static_cast<uint32_t>(r & 7)) << 4), sr[4 * i],
-                   sr[4 * i + 1], sr[4 * i + 2], sr[4 * i + 3]);
-          fence_proxy_async_smem();  // the PV MMA reads it through the async proxy
-        } else {
-          uint32_t pr[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pr[i] = sr[i];
-          tmem_st2_x32<32>(t_p, pr);
-        }
+        for (int i = 0; i < 32; ++i) pr[i] = sr[i];
+        tmem_st2_x32<32>(t_p, pr);
       }
-      if constexpr (!C::SEP) {
+      if constexpr (!C::SEP && FP8) {
+        // P~ as E4M3 of p * ps, ps = 256 * sv_j / sv_max (<= 256): the V block scale rides on P~ so
+        // that U accumulates in one unit for every key tile; ps is folded into the exponent,
+        // p * ps = 2^(s c - m + log2 ps).  Four keys a column: the row's 32 packed columns of S_t
+        // (K block kk of 32 keys at column 8kk), which its thread has read.
+        const float ps = 256.f * sv_j / sv_max;
+        inv_ps = sv_max / (256.f * sv_j);
+        const uint64_t nmp2 = f2_pack(log2f(ps) - mb, log2f(ps) - mb);
+        uint32_t p8[32];
+        auto pack4 = [&](const uint32_t* src4) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(src4[0]), __uint_as_float(src4[1])), c2, nmp2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(src4[2]), __uint_as_float(src4[3])), c2, nmp2), x2, x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          rs_a = f2_add(rs_a, f2_pack(p0, p1));
+          rs_b = f2_add(rs_b, f2_pack(p2, p3));
+          return pack_e4m3x4(p0, p1, p2, p3);
+        };
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p8[i] = pack4(sr + 4 * i);        // keys 4i .. 4i + 3
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p8[16 + i] = pack4(sr2 + 4 * i);  // keys 64 + 4i ..
+        tmem_st_x32(t_s, p8);
+      } else if constexpr (!C::SEP) {
         // P~ packed in place into sr[0..31] (and sr2[0..31]), then the row's 64 packed columns of
         // S_t (keys 2i, 2i + 1 at column i), which its thread (or threads) have read
         exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);
@@ -882,7 +871,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         }
       } else {
         if constexpr (C::ONE)
-          store_full_row(o, lse, static_cast<size_t>(bh) * N + row, row < N, o_fp32 != 0, t_o, l_row, m2);
+          store_full_row(o, lse, static_cast<size_t>(bh) * N + row, row < N, o_fp32 != 0, t_o, l_row, m2,
+                         FP8 ? sv_max * (1.f / 256.f) : 1.f);
         else
           store_half_row<D>(o, lse, static_cast<size_t>(bh) * N + row, h, row < N, o_fp32 != 0, t_o, l_row, m2,
                             FP8 ? sv_max * (1.f / 256.f) : 1.f);

@@ -105,8 +105,8 @@ struct FwdCfg {
   // short for one issuing thread); with P~ aliasing S (bf16, d = 128) one MMA warp alternating
   // between the tiles measured faster.
   static constexpr bool TWO_ISSUERS = SEP;
-  // Softmax warps per query tile: with P~ aliasing S (bf16, d = 128) one thread per row (4 warps,
-  // .32x32b TMEM access); the separate-P~ schedules two threads per row (8 warps, .16x32bx2).
+  // Softmax warps per query tile: with P~ aliasing S (d = 128) one thread per row (4 warps,
+  // .32x32b TMEM access); the separate-P~ schedule (d = 64) two threads per row (8 warps, .16x32bx2).
   static constexpr bool ONE = !SEP;
   static constexpr int SMW = ONE ? 4 : 8;
   static constexpr int WARP_MMA = 2 * SMW;
@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
     // Q block scale (read only for a tile inside N: the scale array has ceil(N/128) entries per head)
     const float sq_t = (FP8 && n > 0) ? sq[static_cast<size_t>(bh) * n_kt + pair * 2 + t] : 1.f;
     const float sv_max = FP8 ? *sv_max_slot : 1.f;
-    float m2 = -INFINITY, l = 0.f;  // l: this thread's half of the row
+    float m2 = -INFINITY, l = 0.f;  // l: this thread's part of the row sum (all of it, one thread a row)
     bool ok = n > 0;
     // FP8: key tile j's K and V block scales, loaded one step ahead
     const float* sk_h = FP8 ? sk + static_cast<size_t>(bh) * n_kt : nullptr;
@@ -809,28 +809,20 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::THREADS, 1)
         for (int i = 0; i < 16; ++i) p8[16 + i] = pack4(sr2 + 4 * i);  // keys 64 + 4i ..
         tmem_st_x32(t_s, p8);
       } else if constexpr (!C::SEP) {
-        // P~ packed in place into sr[0..31] (and sr2[0..31]), then the row's 64 packed columns of
-        // S_t (keys 2i, 2i + 1 at column i), which its thread (or threads) have read
+        // P~ packed in place into sr[0..31] and sr2[0..31], then the row's 64 packed columns of
+        // S_t (keys 2i, 2i + 1 at column i), which its thread has read
         exp_pack_bf16(sr, c2, nmb2, rs_a, rs_b);
-        if constexpr (C::ONE) {
-          exp_pack_bf16(sr2, c2, nmb2, rs_a, rs_b);
-          tmem_st_x32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(sr));         // keys 0..63
-          tmem_st_x32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(sr2));   // keys 64..127
-        } else {
-          uint32_t pr[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pr[i] = sr[i];
-          tmem_st2_x32<32>(t_s, pr);
-        }
+        exp_pack_bf16(sr2, c2, nmb2, rs_a, rs_b);
+        tmem_st_x32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(sr));         // keys 0..63
+        tmem_st_x32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(sr2));   // keys 64..127
       }
       float s0, s1, s2, s3;
       f2_unpack(rs_a, s0, s1);
       f2_unpack(rs_b, s2, s3);
       l = fmaf(alpha, l, ((s0 + s1) + (s2 + s3)) * inv_ps);
       // PV_t(j-1) is complete (the commit that announced S_t(j) covers it): rescale U_t in place.
-      if (!C::SEP && j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
-        if constexpr (C::ONE) rescale_row128(t_o, alpha);
-        else rescale_half_row<D>(t_o, alpha);
+      if constexpr (!C::SEP) {
+        if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) rescale_row128(t_o, alpha);
       }
       tmem_wait_st();
       tc_fence_before();

@@ -346,7 +346,8 @@ __device__ __forceinline__ void stage_full_row_bf16(uint32_t box0, uint32_t box1
   fence_proxy_async_smem();
 }
 
-// One thread per row (d = 128): O row = U / l (fp32 or bf16) and lse to global memory, rows < N.
+// One thread per row (d = 128): O row = U * o_mult / l (fp32 or bf16; o_mult carries the E4M3 V
+// scale) and lse to global memory, rows < N.
 __device__ __forceinline__ void store_full_row(void* o, float* lse, size_t row_off, bool valid, bool o_fp32,
                                                uint32_t taddr, float l, float m2, float o_mult) {
   const float inv = (l > 0.f) ? o_mult / l : 0.f;

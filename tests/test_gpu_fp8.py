@@ -164,6 +164,13 @@ def test_fp8_forward_ragged_sampled_rows():
     _run_and_check(q, k, v, w.scale, True, rows_per_head=8, seed=6)
 
 
+def test_fp8_forward_long_noncausal_sampled_rows():
+    # N = 8189 non-causal with x8 key spikes: every block scans all 64 key tiles, the last ragged
+    from exact_attention_06_gb300 import inputs
+    q, k, v = inputs.prefill_inputs(1, 3, 8189, 128, seed=81, device="cuda", spike=True)
+    _run_and_check(q, k, v, 1 / math.sqrt(128), False, rows_per_head=16, seed=7)
+
+
 def test_fp8_rejects_d64_on_device():
     from exact_attention_06_gb300 import fattn
     x = torch.zeros(1, 1, 128, 64, dtype=torch.uint8, device="cuda")

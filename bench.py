@@ -65,7 +65,7 @@ def _peaks():
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures summarised
 # under profiles/, keyed by kernel and workload, valid only while the kernel sources are unchanged.
 _FWD = "bf5065744ca54e1b253c2dc98ec99b932f320522aa698fdb3178cb9e91562e04"
-_BWD = "20ec4290b32d00271b2f23aa2b70d8c1840fd86b49f539c0a1b0e59c4994df2c"
+_BWD = "3100608144e05a1479f6d4eec6fe754549bc5e11c799049f40b136280dca76b6"
 _DEC = "238a9c1b2ffecb15b22cb24a1544220a197fcbdb2c867899597a0c8e4fa65d64"
 NCU_TRAFFIC = {
     ("fwd_kernel", "ragged"): {"sources": {"fa_fwd.cu": _FWD}, "bytes": 559.377e6},
@@ -73,7 +73,7 @@ NCU_TRAFFIC = {
     ("fwd_kernel_fp8", "causal"): {"sources": {"fa_fwd.cu": _FWD}, "bytes": 136.481e6},
     ("fwd_persist_kernel", "prefill"): {"sources": {"fa_fwd.cu": _FWD}, "bytes": 50.483e6},
     # backward: the dominant kernel (dK/dV) on the causal workload
-    ("bwd_dkdv_kernel", "causal"): {"sources": {"fa_bwd.cu": _BWD}, "bytes": 373.068e6},
+    ("bwd_dkdv_kernel", "causal"): {"sources": {"fa_bwd.cu": _BWD}, "bytes": 372.482e6},
     # the four-shard step: four forward launches over the key shards and the combine, summed
     ("causal_sharded4", "causal"): {"sources": {"fa_fwd.cu": _FWD, "fa_decode.cu": _DEC}, "bytes": 1108.970e6},
     # decode: captured on the B4 slice (decode_small) and scaled by 16 to B64 (K/V streamed once)

@@ -208,8 +208,9 @@ __device__ __forceinline__ void issue_grad_part(uint32_t d_tmem, uint32_t a_tmem
   }
 }
 
-// G (+)= X Y for chunk c of the one-thread-per-row dK/dV kernel (d = 128): K blocks 2c, 2c + 1,
-// packed at columns 8kk (each thread packs its chunk c into columns 16c .., which it has read).
+// G (+)= X Y for chunk c of the one-thread-per-row kernels (d = 128: dK, dV from P^T, dS^T; dQ from
+// dS): K blocks 2c, 2c + 1, packed at columns 8kk (each thread packs its chunk c into columns
+// 16c .., which it has read).
 __device__ __forceinline__ void issue_grad_chunk(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idesc,
                                                  bool accumulate, int c) {
 #pragma unroll
@@ -301,8 +302,8 @@ struct DkdvCfg : BwdCfg<D> {
   static constexpr uint32_t OFF_BAR = OFF_VEC + B::ST * B::VEC;
   // d = 64 takes each query tile in two halves of 64 queries (see the MMA issuer); d = 128 whole.
   static constexpr bool HALVES = D == 64;
-  // B_SF (+ q): products (of query half q) ready; B_PF + c: elementwise chunk (half) c done;
-  // B_GF: gradients final
+  // B_SF (+ q): products (of query half q) ready; B_PF + c: elementwise chunk c done (d = 128:
+  // four 32-query chunks; d = 64: the two query halves); B_GF: gradients final
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = B_FULL + B::ST, B_SF = B_EMPTY + B::ST, B_PF = B_SF + 2,
                        B_GF = B_PF + 4, B_DRAIN = B_GF + 1, B_OW = B_DRAIN + 1, NBAR = B_OW + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8u * NBAR;

@@ -810,9 +810,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    # ~0.3 s timed at the headline's ~1.45 ms a step: enough for clock samples, and a burst like the
-    # measured peak it is divided by (seconds of back-to-back launches run into the power cap)
-    ap.add_argument("--steps", type=int, default=200)
+    # ~30 ms timed at the headline's ~1.45 ms a step: a burst like the measured bf16 peak the
+    # roofline divides by (the best of ten back-to-back GEMMs); longer runs settle under the power
+    # cap, which the clocks record names (sw_power_cap)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--extra-steps", type=int, default=20)
